@@ -1,0 +1,223 @@
+"""Seeded synthetic workloads for the sparse KV assembly path (inputs only).
+
+Both the CPU oracle and the CUDA library are fed from this module; it holds none
+of the method's arithmetic (no probe, no LRU rule, no slot assignment).  It
+provides:
+
+* ``Workload`` -- the shapes of the evaluation points on the pages (16K to 1M
+  token contexts, 20% / 40% fresh Top-k picks, batches up to 192; "XM-Sparse:
+  Netpreme X-Mem ...", TL;DR and test-platform sections) plus small cases that
+  finish in seconds on a CPU.
+* ``fill_rows`` / ``fill_request`` -- deterministic bf16 KV rows (576 elements:
+  a 512-wide latent plus 64 rope dims, 1152 bytes).
+* ``TopkStream`` -- per-step Top-k index rows [B][L][k] (int32, -1 = padding).
+
+The C source is compiled into ``libskv_workload.so`` next to this file by
+``build()``.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "skv_workload.c")
+_LIB = os.path.join(_HERE, "libskv_workload.so")
+
+ROW_ELEMS = 576          # MLA latent 512 + rope 64
+ROW_BYTES = ROW_ELEMS * 2  # bf16
+
+DIST_UNIFORM, DIST_RECENCY, DIST_ZIPF = 0, 1, 2
+ORDER_SORTED, ORDER_SHUFFLED = 0, 1
+
+
+def build(force: bool = False) -> str:
+    """Compile the generator (plain C, OpenMP) in place; return the .so path."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+               "-Wall", "-Wextra", "-o", _LIB + ".tmp", _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(_LIB + ".tmp", _LIB)
+    return _LIB
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(_LIB)
+        u8p = ctypes.c_void_p
+        L.skvw_splitmix64_at.restype = ctypes.c_uint64
+        L.skvw_splitmix64_at.argtypes = [ctypes.c_uint64, ctypes.c_uint64]
+        L.skvw_key.restype = ctypes.c_uint64
+        L.skvw_key.argtypes = [ctypes.c_uint64] * 5
+        L.skvw_fill_rows.restype = None
+        L.skvw_fill_rows.argtypes = [u8p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_int32,
+                                     ctypes.c_int64, ctypes.c_int64, ctypes.c_int32]
+        L.skvw_fill_request.restype = None
+        L.skvw_fill_request.argtypes = [u8p, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
+                                        ctypes.c_uint64, ctypes.c_uint64, ctypes.c_int32]
+        L.skvw_topk_create.restype = ctypes.c_void_p
+        L.skvw_topk_create.argtypes = [ctypes.c_int32] * 8 + [ctypes.c_double, ctypes.c_int32, ctypes.c_int32,
+                                                               ctypes.c_double, ctypes.c_uint64, ctypes.c_int64]
+        L.skvw_topk_destroy.restype = None
+        L.skvw_topk_destroy.argtypes = [ctypes.c_void_p]
+        L.skvw_topk_reset.restype = None
+        L.skvw_topk_reset.argtypes = [ctypes.c_void_p, ctypes.c_int32]
+        L.skvw_topk_step.restype = ctypes.c_int32
+        L.skvw_topk_step.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
+                                     ctypes.c_int32]
+        _lib = L
+    return _lib
+
+
+def default_threads() -> int:
+    return max(1, min(32, os.cpu_count() or 1))
+
+
+def splitmix64_at(key: int, c: int) -> int:
+    return int(lib().skvw_splitmix64_at(key, c))
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    """One synthetic decode workload.
+
+    B requests x L layers; each request starts with ``ctx`` tokens in the host
+    pool (``max_context`` leaves room for appended tokens); each (request,
+    layer) selects ``k`` tokens per step into a hot buffer of ``S`` slots.
+    ``n_fresh`` of the ``k - n_pad`` selected tokens are drawn fresh each step,
+    the rest are kept from the previous step's selection.
+    """
+    name: str
+    B: int
+    L: int
+    ctx: int
+    k: int
+    S: int
+    steps: int
+    fresh: float = 0.2
+    dist: int = DIST_UNIFORM
+    order: int = ORDER_SORTED
+    n_pad: int = 0
+    window: int = 2048
+    p_window: float = 0.7
+    block: int = 64
+    zipf_s: float = 1.1
+    appends: bool = False           # one write_back per request per step
+    lifecycle_step: int = -1        # release + publish of batch entry 1 before this step
+    max_requests: int = 0           # 0 -> B
+    seed: int = 0
+
+    @property
+    def R(self) -> int:
+        return self.max_requests or self.B
+
+    @property
+    def n_fresh(self) -> int:
+        # round(f * kv), halves away from zero
+        return int(self.fresh * (self.k - self.n_pad) + 0.5)
+
+    @property
+    def max_context(self) -> int:
+        return self.ctx + (self.steps if self.appends else 0)
+
+    @property
+    def base_seed(self) -> int:
+        return self.seed if self.seed else (0x5EED0000 + sum(map(ord, self.name)))
+
+    def pool_bytes(self) -> int:
+        return self.R * self.L * self.max_context * ROW_BYTES
+
+    def hot_bytes(self) -> int:
+        return self.R * self.L * self.S * ROW_BYTES
+
+    def req_key(self, b: int, generation: int = 0) -> int:
+        """Key of the KV contents of batch entry b (a re-published request gets
+        a new generation and so new contents)."""
+        return b + (generation << 32)
+
+
+# The evaluation points.  c1..c5 are the five configurations of the build
+# contract; "target" is the pages' headline point (16K context, 20% miss,
+# batch 192 per GPU), which none of c1..c5 matches exactly.
+WORKLOADS = {
+    "c1_tiny": Workload("c1_tiny", B=4, L=1, ctx=4096, k=256, S=512, steps=64, fresh=0.2),
+    "c2_16k_b64_append": Workload("c2_16k_b64_append", B=64, L=8, ctx=16384, k=2048, S=4096, steps=128,
+                                  fresh=0.2, appends=True),
+    "c3_16k_b192_f40_recency": Workload("c3_16k_b192_f40_recency", B=192, L=8, ctx=16384, k=2048, S=4096,
+                                        steps=128, fresh=0.4, dist=DIST_RECENCY),
+    "c4_128k_b32_zipf": Workload("c4_128k_b32_zipf", B=32, L=4, ctx=131072, k=2048, S=4096, steps=64,
+                                 fresh=0.2, dist=DIST_ZIPF),
+    "c5_1m_b4_lifecycle": Workload("c5_1m_b4_lifecycle", B=4, L=4, ctx=1048576, k=2048, S=8192, steps=64,
+                                   fresh=0.2, lifecycle_step=32),
+    "target_16k_b192_f20": Workload("target_16k_b192_f20", B=192, L=8, ctx=16384, k=2048, S=4096, steps=128,
+                                    fresh=0.2),
+}
+
+
+def fill_rows(seed: int, req_key: int, layer: int, t0: int, n: int, row_elems: int = ROW_ELEMS) -> np.ndarray:
+    """KV rows of tokens [t0, t0+n) as a uint8 array [n][row_elems*2]."""
+    out = np.empty((n, row_elems * 2), dtype=np.uint8)
+    if n:
+        lib().skvw_fill_rows(out.ctypes.data, row_elems * 2, seed, req_key, layer, t0, n, row_elems)
+    return out
+
+
+def fill_rows_into(ptr: int, stride: int, seed: int, req_key: int, layer: int, t0: int, n: int,
+                   row_elems: int = ROW_ELEMS) -> None:
+    lib().skvw_fill_rows(ptr, stride, seed, req_key, layer, t0, n, row_elems)
+
+
+def fill_request(req_base_ptr: int, L: int, T_max: int, T: int, seed: int, req_key: int,
+                 row_elems: int = ROW_ELEMS, nthreads: int | None = None) -> None:
+    """Write rows [0, T) of every layer of one request into a pool region laid
+    out [L][T_max][row_elems*2] at host address ``req_base_ptr``."""
+    lib().skvw_fill_request(req_base_ptr, L, T_max, T, row_elems, seed, req_key,
+                            nthreads or default_threads())
+
+
+class TopkStream:
+    """Per-step Top-k rows for a workload: ``step(s, lens)`` -> int32 [B][L][k]."""
+
+    def __init__(self, w: Workload, nthreads: int | None = None):
+        self.w = w
+        self.nthreads = nthreads or default_threads()
+        nblocks = max(1, w.ctx // w.block)
+        self._g = lib().skvw_topk_create(w.B, w.L, w.k, w.n_fresh, w.n_pad, w.dist, w.order, w.window,
+                                         w.p_window, w.block, nblocks, w.zipf_s, w.base_seed, w.max_context)
+        if not self._g:
+            raise ValueError(f"bad workload {w}")
+
+    def step(self, s: int, lens, out: np.ndarray | None = None) -> np.ndarray:
+        w = self.w
+        lens = np.ascontiguousarray(np.asarray(lens, dtype=np.int64))
+        assert lens.shape == (w.B,)
+        if out is None:
+            out = np.empty((w.B, w.L, w.k), dtype=np.int32)
+        assert out.dtype == np.int32 and out.flags.c_contiguous and out.shape == (w.B, w.L, w.k)
+        rc = lib().skvw_topk_step(self._g, s, lens.ctypes.data, out.ctypes.data, self.nthreads)
+        if rc != 0:
+            raise ValueError("top-k generation failed (context shorter than k?)")
+        return out
+
+    def reset(self, b: int) -> None:
+        lib().skvw_topk_reset(self._g, b)
+
+    def close(self) -> None:
+        if self._g:
+            lib().skvw_topk_destroy(self._g)
+            self._g = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

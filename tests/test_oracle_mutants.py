@@ -1,0 +1,91 @@
+"""Planted mistakes in the oracle must each be caught by its pins.
+
+Each case copies the oracle source, applies one small edit that models a
+plausible implementation mistake (a wrong tie-break, a missing sort, a dropped
+map update, a wrong source row, ...), compiles the copy and runs the pins on it
+(CPU only).  The test passes when at least one pin fails for every mutant, i.e.
+no such mistake could hide behind the current pins.
+"""
+import concurrent.futures as cf
+import os
+import tempfile
+
+import pytest
+
+import oracle as orc
+import skv_workload as wl
+import oracle_pins as pins
+
+MUTANTS = {
+    "tie_break_highest_slot": [
+        ("for (int32_t s = 0; s < o->S; ++s) u.lru.push_back(s);",
+         "for (int32_t s = o->S - 1; s >= 0; --s) u.lru.push_back(s);")],
+    "misses_in_row_order": [
+        ("std::sort(missing.begin(), missing.end());", "/* no sort */")],
+    "misses_descending": [
+        ("std::sort(missing.begin(), missing.end());",
+         "std::sort(missing.begin(), missing.end(), [](auto a, auto b) { return a > b; });")],
+    "hits_evictable_and_not_refreshed": [
+        ("u.lru.remove_if([&](int32_t s) { return hit_set.count(s) != 0; });", "/* hits stay */"),
+        ("std::vector<int32_t> touched(hit_slots);", "std::vector<int32_t> touched;")],
+    "hit_stamp_not_updated": [
+        ("u.ts[s] = now;",
+         "if (std::find(victims.begin(), victims.end(), s) != victims.end()) u.ts[s] = now;")],
+    "evicted_token_kept_in_map": [
+        ("if (old >= 0) u.tok2slot.erase(old);", "(void)old;")],
+    "wrong_source_row": [
+        ("pool_row(o, q, u, r, l, t), o->row_bytes);", "pool_row(o, q, u, r, l, t > 0 ? t - 1 : t), o->row_bytes);")],
+    "clock_advances_on_reject": [
+        ("        o->err |= e;\n        reject();\n        return e;",
+         "        o->err |= e;\n        o->now += 1;\n        reject();\n        return e;")],
+    "duplicates_not_checked": [
+        ("else if (!row_tokens.insert(t).second) e |= E_DUPLICATE;", "else row_tokens.insert(t);")],
+    "touched_not_in_slot_order": [
+        ("std::sort(touched.begin(), touched.end());", "/* no sort */")],
+    "victims_from_back": [
+        ("victims.push_back(u.lru.front());\n        u.lru.pop_front();",
+         "victims.push_back(u.lru.back());\n        u.lru.pop_back();")],
+    "write_back_no_len_increment": [
+        ("        q.len += 1;\n", "")],
+    "sticky_error_ignored": [
+        ("    if (o->err) {\n        reject();\n        return o->err;\n    }", "")],
+}
+
+
+def _build(name, edits, tmp):
+    src = open(orc.SRC).read()
+    for old, new in edits:
+        assert src.count(old) == 1, (name, old)
+        src = src.replace(old, new)
+    p = os.path.join(tmp, f"{name}.cpp")
+    open(p, "w").write(src)
+    return orc.compile_oracle(p, os.path.join(tmp, f"lib{name}.so"))
+
+
+def _caught(lib_path):
+    checks = [
+        lambda: pins.check_golden(lib_path),
+        lambda: pins.check_closed_forms(lib_path),
+        lambda: pins.check_errors(lib_path),
+        lambda: pins.check_bruteforce(lib_path, T=4, k=2, S_values=(2, 3), steps=3, variant="ordered"),
+        lambda: pins.check_invariants(wl.Workload("mut_inv", B=2, L=1, ctx=100, k=12, S=20, steps=6, fresh=0.4,
+                                                  order=wl.ORDER_SHUFFLED), lib_path),
+    ]
+    for c in checks:
+        try:
+            c()
+        except (AssertionError, IndexError, KeyError, ValueError):
+            return True
+    return False
+
+
+def test_every_planted_mistake_is_caught():
+    with tempfile.TemporaryDirectory() as tmp:
+        with cf.ThreadPoolExecutor(max_workers=os.cpu_count() or 2) as ex:
+            libs = dict(zip(MUTANTS, ex.map(lambda kv: _build(kv[0], kv[1], tmp), MUTANTS.items())))
+        missed = [name for name, lib in libs.items() if not _caught(lib)]
+    assert not missed, f"pins did not catch: {missed}"
+
+
+def test_unmodified_oracle_passes_the_same_checks():
+    assert not _caught(orc.build())
