@@ -1,0 +1,466 @@
+"""Benchmark of the skv_assemble step (sparse KV assembly) on GB300.
+
+One step = one skv_assemble call over a batch of B requests x L layers with k
+Top-k entries each: validate, sparse diff, LRU slot allocation, gather of the
+missed rows from the pinned host pool into the HBM hot buffer, slot emission.
+Workloads that append (write back) include one skv_write_back per step.
+
+Prints ONE JSON line.  ``value`` is missed-KV GB/s over the timed steps
+(missed rows x row bytes / device time); inputs (Top-k rows for every step)
+are resident in HBM before the timed region, and the per-step footprint
+(hot-buffer writes + maps) is far larger than L2.  ``e2e`` is the same metric
+through the host-buffer entry point skv_assemble_host, with the per-step
+host->device and device->host copies inside the timed region.
+
+  python bench.py [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+  torchrun --nproc-per-node N bench.py --gpus N ...   (weak scaling: one replica per GPU)
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import skv_workload as wl  # noqa: E402
+
+METRIC = "missed-KV GB/s per skv_assemble step (host pool -> HBM hot buffer)"
+DEFAULT_WORKLOAD = "target_16k_b192_f20"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of per-step CUDA graphs")
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--cpu-sample-requests", type=int, default=32)
+    ap.add_argument("--cpu-sample-steps", type=int, default=24)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed harness (weak scaling: each rank runs its own replica)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return ws, rank, local
+
+
+def init_dist(ws):
+    if ws <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group("gloo")
+    return dist
+
+
+def rank_seed(w: wl.Workload, rank: int) -> wl.Workload:
+    """Each rank's replica gets its own seed: independent problems."""
+    import dataclasses
+    return dataclasses.replace(w, seed=w.base_seed + 7919 * rank)
+
+
+def reduce_results(dist, elapsed_s: float, missed_bytes: float, tokens: float):
+    """Max of the elapsed time and sums of the work over ranks."""
+    if dist is None:
+        return elapsed_s, missed_bytes, tokens
+    import torch
+    t = torch.tensor([elapsed_s], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    s = torch.tensor([missed_bytes, tokens], dtype=torch.float64)
+    dist.all_reduce(s, op=dist.ReduceOp.SUM)
+    return float(t[0]), float(s[0]), float(s[1])
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: int, enabled: bool = True):
+        self.device = device
+        self.p = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        if enabled:
+            try:
+                os.makedirs(os.path.dirname(self.path), exist_ok=True)
+                self.f = open(self.path, "w")
+                self.p = subprocess.Popen(["nvidia-smi", "-i", str(device), f"--query-gpu={self.QUERY}",
+                                           "--format=csv,noheader,nounits", "-lms", "50"],
+                                          stdout=self.f, stderr=subprocess.DEVNULL)
+            except Exception:
+                self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return None
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[2]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# measurements
+# ---------------------------------------------------------------------------
+
+def measure_link_gbs(torch, dev):
+    """Pinned cudaMemcpyAsync host->device and device->host, 1 GiB, best of 10."""
+    n = 1 << 30
+    h = torch.empty(n, dtype=torch.uint8).pin_memory()
+    d = torch.empty(n, dtype=torch.uint8, device=dev)
+    s = torch.cuda.current_stream()
+    out = {}
+    for name, (dst, src) in {"h2d": (d, h), "d2h": (h, d)}.items():
+        best = 1e9
+        for _ in range(10):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            dst.copy_(src, non_blocking=True)
+            b.record(s)
+            b.synchronize()
+            best = min(best, a.elapsed_time(b) / 1e3)
+        out[name] = n / best / 1e9
+    del h, d
+    return out
+
+
+def hbm_peak_gbs():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            return float(json.load(open(p))["hbm_gbs"]), "MEASURED_PEAKS.json hbm_gbs (measured copy)"
+        except Exception:
+            pass
+    return 6800.0, "fallback 6.8 TB/s"
+
+
+def hbm_algorithmic_bytes(w: wl.Workload, M: int, hits: int) -> int:
+    """Bytes one step must move in HBM (besides the link reads): Top-k read,
+    tok2slot probes, slot tensor write, LRU order read+write, clock stamps of
+    used slots, map updates of the misses, and the missed rows written."""
+    U = w.B * w.L
+    return (U * w.k * 4 * 3 + U * w.S * 2 * 2 + (hits + M) * 4 + M * 16 + M * wl.ROW_BYTES)
+
+
+def cpu_baseline(w: wl.Workload, pool_addr: int | None, n_req: int, n_steps: int, warm: int = 2):
+    """The oracle as it stands, on this host's cores, over the first n_req
+    requests of the workload for n_steps steady-state steps (after `warm`
+    steps, the first of which is cold).  Returns (GB/s, tokens/s, info)."""
+    import oracle as orc
+    n_req = min(n_req, w.B)
+    T_max = w.max_context
+    rb = wl.ROW_BYTES
+    own = None
+    if pool_addr is None:
+        own = np.empty(n_req * w.L * T_max * rb, dtype=np.uint8)
+        pool_addr = own.ctypes.data
+        for r in range(n_req):
+            wl.fill_request(pool_addr + r * w.L * T_max * rb, w.L, T_max, w.ctx, w.base_seed, w.req_key(r))
+    threads = os.cpu_count() or 1
+    o = orc.Oracle(n_req, w.L, T_max, rb, w.k, w.S, pool_addr if own is None else own)
+    for r in range(n_req):
+        assert o.publish(w.ctx) == r
+    import dataclasses
+    ws = dataclasses.replace(w, B=n_req)
+    gen = wl.TopkStream(ws)
+    lens = [w.ctx] * n_req
+    req = list(range(n_req))
+    tot_t, tot_m, tot_tok = 0.0, 0, 0
+    for s in range(warm + n_steps):
+        topk = gen.step(s, lens)
+        t0 = time.perf_counter()
+        e, slots, hits, misses = o.assemble(req, topk, nthreads=threads)
+        dt = time.perf_counter() - t0
+        assert e == 0
+        if s >= warm:
+            tot_t += dt
+            tot_m += int(misses.sum())
+            tot_tok += int(hits.sum() + misses.sum())
+    o.close()
+    gen.close()
+    return (tot_m * rb / tot_t / 1e9, tot_tok / tot_t,
+            {"cores": threads, "sample": f"{n_req} of {w.B} requests x {w.L} layers, {n_steps} steady-state steps "
+                                        f"after {warm} warm-up steps (first cold), {w.name}",
+             "seconds": tot_t})
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    ws, rank, local = dist_env()
+    dist = init_dist(ws)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import __graft_entry__
+    __graft_entry__.build()
+    from sparse_attention_kv_skv_gb300 import Config, Context
+
+    w = rank_seed(wl.WORKLOADS[args.workload], rank)
+    rb = wl.ROW_BYTES
+    T_max = w.max_context
+    W, K = args.warmup, args.steps
+    assert W >= 1
+
+    link = measure_link_gbs(torch, dev)
+    hbm_peak, hbm_src = hbm_peak_gbs()
+
+    ctx = Context(Config(max_requests=w.B, num_layers=w.L, max_context=T_max, topk=w.k, hot_slots=w.S,
+                         max_batch=w.B, row_bytes=rb, device=local))
+    pool = ctx.pool_rows()
+    for r in range(w.B):
+        assert ctx.publish(w.ctx) == r
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for r in range(w.B):
+        wl.fill_request(pool + r * w.L * T_max * rb, w.L, T_max, w.ctx, w.base_seed, w.req_key(r))
+    fill_s = time.time() - t0
+
+    # inputs for every step, resident in HBM before timing
+    gen = wl.TopkStream(w)
+    lens = [w.ctx] * w.B
+    n_dev = W + K
+    topk_all = torch.empty((n_dev, w.B, w.L, w.k), dtype=torch.int32, device=dev)
+    wb_rows = None
+    host_steps = []
+    for s in range(n_dev + args.e2e_steps):
+        x = gen.step(s, [l + (s if w.appends else 0) for l in lens])
+        if s < n_dev:
+            topk_all[s].copy_(torch.from_numpy(x))
+        else:
+            host_steps.append(torch.from_numpy(x).pin_memory())
+    if w.appends:
+        # the appended rows' contents do not affect timing: one fixed block per step
+        wb_rows = torch.zeros((w.B, w.L, rb), dtype=torch.uint8, device=dev)
+    req = torch.arange(w.B, dtype=torch.int32, device=dev)
+    slots = torch.empty((w.B, w.L, w.k), dtype=torch.int32, device=dev)
+    hits = torch.empty((n_dev, w.B, w.L), dtype=torch.int32, device=dev)
+    misses = torch.empty((n_dev, w.B, w.L), dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    ev_b = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n_dev)]
+    ev_a = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n_dev)]
+
+    def enqueue(s):
+        ctx.set_gather_events(ev_b[s], ev_a[s])
+        ctx.assemble(req, topk_all[s], slots, hits[s], misses[s], stream=stream.cuda_stream)
+        if w.appends:
+            ctx.write_back(req, wb_rows, stream=stream.cuda_stream)
+
+    graphs = []
+    use_graph = not args.no_graph
+    if use_graph:
+        # warm-up steps run eagerly; timed steps are one captured graph each
+        with torch.cuda.stream(stream):
+            for s in range(W, n_dev):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    enqueue(s)
+                graphs.append(g)
+        ctx.set_gather_events(None, None)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for s in range(W):
+            enqueue(s)
+    torch.cuda.synchronize()
+    st0 = ctx.stats()
+    if dist is not None:
+        dist.barrier()
+    sampler = ClockSampler(local, enabled=not args.no_clocks)
+    time.sleep(0.2 if not args.no_clocks else 0)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for i, s in enumerate(range(W, n_dev)):
+            if use_graph:
+                graphs[i].replay()
+            else:
+                enqueue(s)
+        end.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    elapsed = start.elapsed_time(end) / 1e3
+    st1 = ctx.stats()
+    M = st1["misses"] - st0["misses"]
+    H = st1["hits"] - st0["hits"]
+    assert st1["calls"] - st0["calls"] == K
+    assert ctx.get_device_error() == 0
+    gather_s = sum(ev_b[s].elapsed_time(ev_a[s]) for s in range(W, n_dev)) / 1e3
+    per_step_m = misses[W:].sum(dim=(1, 2)).cpu().numpy().astype(np.int64)
+    per_step_h = hits[W:].sum(dim=(1, 2)).cpu().numpy().astype(np.int64)
+    assert int(per_step_m.sum()) == M
+    tokens = float(H + M)
+
+    # step roofline: slower of link and HBM terms, per step
+    t_roof = 0.0
+    for m_s, h_s in zip(per_step_m, per_step_h):
+        t_roof += max(m_s * rb / (link["h2d"] * 1e9), hbm_algorithmic_bytes(w, int(m_s), int(h_s)) / (hbm_peak * 1e9))
+
+    # end to end through the host-buffer entry point
+    e2e = None
+    if args.e2e_steps > 0:
+        req_h = torch.arange(w.B, dtype=torch.int32).pin_memory()
+        slots_h = torch.empty((w.B, w.L, w.k), dtype=torch.int32).pin_memory()
+        hits_h = torch.empty((w.B, w.L), dtype=torch.int32).pin_memory()
+        misses_h = torch.empty((w.B, w.L), dtype=torch.int32).pin_memory()
+        m_e2e = 0
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for x in host_steps:
+            ctx.assemble_host(req_h, x, slots_h, hits_h, misses_h, stream=stream.cuda_stream)
+            if w.appends:
+                ctx.write_back(req, wb_rows, stream=stream.cuda_stream)
+            m_e2e += int(misses_h.sum())
+        torch.cuda.synchronize()
+        e2e_s = time.perf_counter() - t0
+        e2e = {"value": m_e2e * rb / e2e_s / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": w.B * 4 + w.B * w.L * w.k * 4,
+               "d2h_bytes_per_step": w.B * w.L * w.k * 4 + 2 * w.B * w.L * 4,
+               "ms_per_step": 1e3 * e2e_s / len(host_steps), "steps": len(host_steps),
+               "entry_point": "skv_assemble_host (pinned host buffers; copies + sync inside the timed region)"}
+
+    elapsed_max, bytes_all, tokens_all = reduce_results(dist, elapsed, float(M * rb), tokens)
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        gbs, tps, info = cpu_baseline(w, pool, args.cpu_sample_requests, args.cpu_sample_steps)
+        cpu = {"value": gbs, "unit": "GB/s", "cores": info["cores"], "kind": "oracle", "sample": info["sample"],
+               "assembled_tokens_per_s": tps}
+    if rank == 0:
+        achieved = M * rb / gather_s / 1e9
+        out = {
+            "metric": METRIC,
+            "value": bytes_all / elapsed_max / 1e9,
+            "unit": "GB/s",
+            "n_gpus": ws,
+            "steps": K,
+            "warmup": W,
+            "ms_per_step": 1e3 * elapsed_max / K,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "int32",
+            "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.B, "layers": w.L, "context": w.ctx, "topk": w.k,
+                       "hot_slots": w.S, "fresh": w.fresh, "row_bytes": rb, "row_dtype": "bf16",
+                       "write_back_per_step": w.appends, "cuda_graph": use_graph,
+                       "l2": "inputs larger than L2: each step writes the missed rows (~0.6 GB) into a "
+                             f"{w.hot_bytes() / 1e9:.2f} GB hot buffer and reads {w.B * w.L * w.max_context * 4 / 1e6:.0f} MB "
+                             "of token->slot maps; no flush"},
+            "assembled_tokens_per_s": tokens_all / elapsed_max,
+            "miss_rate": M / max(tokens, 1.0),
+            "missed_rows_per_step": M / K,
+            "step_roofline_frac": t_roof / elapsed,
+            "roofline": {"bound": "host_link", "kernel": "gather_kernel", "achieved": achieved,
+                         "peak": link["h2d"], "unit": "GB/s", "frac": achieved / link["h2d"], "traffic": None,
+                         "peak_source": "pinned cudaMemcpyAsync host->device, 1 GiB, best of 10, this run",
+                         "gather_share_of_step": gather_s / elapsed,
+                         "hbm": {"peak": hbm_peak, "peak_source": hbm_src,
+                                 "algorithmic_bytes_per_step": sum(hbm_algorithmic_bytes(w, int(a), int(b))
+                                                                   for a, b in zip(per_step_m, per_step_h)) / K}},
+            "link_gbs": link,
+            "e2e": e2e,
+            "gpu_launches": K * (3 + (2 if w.appends else 0)),
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+            "setup": {"pool_gb": w.pool_bytes() / 1e9, "pool_fill_s": fill_s},
+        }
+        print(json.dumps(out), flush=True)
+    ctx.close()
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the CPU oracle, as it stands
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import __graft_entry__  # noqa: F401
+    import oracle
+    oracle.build()
+    wl.build()
+    w = wl.WORKLOADS[args.workload]
+    n_steps = max(1, args.steps if args.steps <= 40 else 40)
+    gbs, tps, info = cpu_baseline(w, None, args.cpu_sample_requests, n_steps, warm=max(1, min(args.warmup, 3)))
+    out = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": gbs,
+        "unit": "GB/s",
+        "n_gpus": ws,
+        "steps": n_steps,
+        "warmup": args.warmup,
+        "ms_per_step": 1e3 * info["seconds"] / n_steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.B, "layers": w.L, "context": w.ctx, "topk": w.k,
+                   "hot_slots": w.S, "fresh": w.fresh, "row_bytes": wl.ROW_BYTES},
+        "assembled_tokens_per_s": tps,
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": info["cores"], "kind": "oracle",
+                         "sample": info["sample"]},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "note": "the reference pages ship no code; this arm times the CPU oracle (plain C++ hash map + LRU "
+                "list + memcpy) on a bounded sample of the same workload",
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,235 @@
+/*
+ * skv.h -- C ABI of the sparse-attention KV assembly library (GB300, sm_103a).
+ *
+ * What the library does.  Long-context decoding keeps the complete KV history
+ * of every request in a host memory pool and only a cache of hot tokens on the
+ * accelerator; each decode step, per layer, the sparse-attention Top-k indices
+ * say which tokens the attention kernel needs, and those tokens are assembled
+ * on the device on demand, at token (not page) granularity:
+ *   - "Sparse Attention-Driven KVCache Management for Domestic AI Supernodes"
+ *     (ml-summit.org talk abstract): abstract, and agenda item 2 (host storage,
+ *     device cache and index mapping of the SparseKVCacheManager; the UniDex
+ *     index-copy operator that keeps the step graph-executable);
+ *   - "SGLang и Tair представили иерархичную Sparse Attention для хранения
+ *     полного KV Cache на CPU и экономии GPU-памяти": paragraph 1 (full KV on
+ *     the CPU, a Top-k LRU buffer on the GPU), paragraph 3 (incremental
+ *     transfer of sparse changes by the Sparse Diff Kernel, fast I/O kernels);
+ *   - "XM-Sparse: Netpreme X-Mem 突破稀疏注意力吞吐极限": section "与SGLang
+ *     HiSparse的集成" (CUDA Graph support; lifecycle publish, acquire, write
+ *     back, release), section "为何稀疏注意力需要快速高容量内存层" (a hot KV
+ *     buffer in HBM reduces external-memory reads).
+ *
+ * Geometry.  R request slots, L layers, T_max tokens of pool room per request,
+ * rows of row_bytes bytes (576 bf16 = 1152 B for an MLA latent of 512 plus 64
+ * rope dims), k Top-k entries per (request, layer) and step, S >= k hot slots
+ * per (request, layer).
+ *
+ * Memory the library owns (all allocated by skv_create, freed by skv_destroy):
+ *   pool  [R][L][T_max][row_bytes]  host memory, pinned and mapped into the
+ *                                   GPU's address space (the host storage)
+ *   hot   [R][L][S][row_bytes]      device memory (the device cache)
+ *   tok2slot [R][L][T_max] int32    device; -1 = token not resident
+ *   slot2tok [R][L][S] int32        device; -1 = empty slot
+ *   ts       [R][L][S] uint32       device; clock of the step that last used the slot (0 = never)
+ *   lru      [R][L][S] uint16       device; the S slots ordered by (ts, slot), least recent first
+ *   len/active per request, the step clock, the sticky error word, and the
+ *   gather work list [max_batch * L * k] -- all device memory.
+ * No call after skv_create allocates; skv_assemble and skv_write_back are
+ * therefore safe to capture in a CUDA graph.
+ *
+ * The replacement rule (the pages name an LRU buffer but not its tie-breaks;
+ * these are the readings this library implements):
+ *   - a global step clock advances by one on every successful skv_assemble;
+ *   - a slot whose token is in this step's Top-k is a hit and is never
+ *     evicted in that step;
+ *   - the missing tokens, in ascending token order, take the non-hit slots
+ *     with the smallest (ts, slot index), in that order;
+ *   - every slot used by the step (hits and fills) gets ts = clock.
+ *
+ * Streams and ordering.  Every call that takes a cudaStream_t only enqueues
+ * work on that stream (plus, where stated, a synchronisation of it).  Calls on
+ * one context must be ordered: issue them on one stream, or order the streams
+ * with events.  Two overlapping calls on one context race.
+ *
+ * Errors.  Each call returns an skv_status.  Errors that the host can see
+ * (bad handle, bad sizes, null pointers, unknown request in skv_release, no
+ * free request slot) are returned at once and nothing is enqueued.  Errors
+ * that depend on device data (bad request ids in a device array, Top-k entries
+ * out of range or repeated, a full pool region) are detected on the device:
+ * the call then changes no state, fills its outputs with -1, and ORs an
+ * SKV_DEVERR_* bit into a sticky device error word.  While that word is
+ * non-zero every later skv_assemble / skv_write_back is a no-op with -1
+ * outputs.  skv_get_device_error reads and clears it.  No kernel traps,
+ * asserts or spins.
+ */
+#ifndef SKV_H_
+#define SKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t / cudaEvent_t without including the CUDA headers (same
+ * underlying types). */
+typedef struct CUstream_st *skv_stream_t;
+typedef struct CUevent_st *skv_event_t;
+
+typedef struct skv_ctx skv_ctx;
+
+/* Every entry point is exported with default visibility; the library is built
+ * with everything else hidden. */
+#if defined(__GNUC__)
+#define SKV_API __attribute__((visibility("default")))
+#else
+#define SKV_API
+#endif
+
+typedef enum {
+    SKV_OK = 0,
+    SKV_ERR_INVALID_ARG = 1,     /* null pointer, bad size or bad configuration */
+    SKV_ERR_OOM = 2,             /* host or device allocation failed in skv_create */
+    SKV_ERR_BAD_REQUEST = 3,     /* skv_release / skv_export_*: request id unknown or not active */
+    SKV_ERR_NO_FREE_REQUEST = 4, /* skv_publish: all R request slots are in use */
+    SKV_ERR_CONTEXT_FULL = 5,    /* skv_publish: T > max_context */
+    SKV_ERR_CUDA = 6             /* a CUDA runtime call failed (see skv_last_cuda_error) */
+} skv_status;
+
+/* Bits of the sticky device error word. */
+#define SKV_DEVERR_BAD_REQUEST 1   /* a request id in [0,R) that is not active, out of range, or repeated in one call */
+#define SKV_DEVERR_BAD_INDEX 2     /* a Top-k entry that is neither -1 nor in [0, len of its request) */
+#define SKV_DEVERR_DUPLICATE 4     /* a token that appears twice in one (request, layer) Top-k row */
+#define SKV_DEVERR_CONTEXT_FULL 8  /* skv_write_back on a request whose pool region holds max_context tokens */
+
+typedef struct {
+    int32_t max_requests;  /* R >= 1: request slots */
+    int32_t num_layers;    /* L >= 1 */
+    int64_t max_context;   /* T_max >= 1: pool rows per (request, layer) */
+    int32_t row_bytes;     /* bytes per KV row; multiple of 16 (1152 for 576 bf16) */
+    int32_t topk;          /* k, 1 <= k <= 4096 */
+    int32_t hot_slots;     /* S, k <= S <= 16384 */
+    int32_t max_batch;     /* largest B of skv_assemble / n of skv_write_back */
+    int32_t device;        /* CUDA device ordinal */
+} skv_config;
+
+/* Create a context: allocates the pinned, mapped host pool
+ * (cudaHostAllocMapped | cudaHostAllocPortable), the device cache and all
+ * device state; every request slot starts free and the hot buffer zeroed.
+ * Requires R*L*T_max < 2^32 and R*L*S < 2^32.  *out receives the handle.
+ * Synchronous.  Returns SKV_ERR_INVALID_ARG for a bad configuration,
+ * SKV_ERR_OOM / SKV_ERR_CUDA on allocation failure (nothing is leaked). */
+SKV_API skv_status skv_create(const skv_config *cfg, skv_ctx **out);
+
+/* Synchronise the device and free everything.  A null ctx is a no-op. */
+SKV_API skv_status skv_destroy(skv_ctx *ctx);
+
+/* Publish a request (lifecycle step "publish"): take the lowest free request
+ * slot, make its pool region hold T tokens, reset its maps and clocks and zero
+ * its hot rows.  rows, if not null, is [L][T][row_bytes] in host or device
+ * memory and is copied into the pool; a host source first synchronises
+ * `stream` (so in-flight reads of a previously released request finish) and
+ * is copied by the CPU.  With rows == null the caller writes the rows in place
+ * through skv_pool_rows before the next skv_assemble on this request.  The
+ * device reset is enqueued on `stream`.  *out_req receives the id.
+ * Errors: SKV_ERR_CONTEXT_FULL (T > max_context), SKV_ERR_NO_FREE_REQUEST. */
+SKV_API skv_status skv_publish(skv_ctx *ctx, const void *rows, int64_t T, int32_t *out_req, skv_stream_t stream);
+
+/* Write back one new token per listed request (lifecycle step "write back"):
+ * for i < n, for each layer l, rows_dev[i][l][:] is stored into the pool at
+ * position len(req_ids_dev[i]) and that length grows by one.  req_ids_dev
+ * [n] int32 and rows_dev [n][L][row_bytes] are device memory (rows may also
+ * be mapped host memory).  Device-side errors: SKV_DEVERR_BAD_REQUEST
+ * (unknown, inactive or repeated id), SKV_DEVERR_CONTEXT_FULL; on error
+ * nothing is written.  The new token can be selected from the next
+ * skv_assemble on; it is not put into the hot buffer by this call.
+ * n == 0 enqueues nothing.  Host errors: n < 0 or n > max_batch, null
+ * pointers with n > 0. */
+SKV_API skv_status skv_write_back(skv_ctx *ctx, const int32_t *req_ids_dev, int32_t n, const void *rows_dev,
+                          skv_stream_t stream);
+
+/* One decode step (lifecycle step "acquire"): for each batch entry b < B and
+ * layer l, make every token of topk_dev[b][l][0..k) resident in the hot
+ * buffer of request req_ids_dev[b], layer l, and write its slot index to
+ * slots_dev[b][l][i] (-1 for a -1 entry).  Steps, all on the device:
+ *   1. validate ids and entries (nothing changes if any is bad);
+ *   2. sparse diff: probe tok2slot; hits keep their slot, misses are
+ *      compacted and ordered by token;
+ *   3. LRU allocation: the misses take the least recently used non-hit slots
+ *      (rule above); evicted tokens leave tok2slot;
+ *   4. gather: copy each missed token's row from the host pool into its slot
+ *      (16-byte loads through the mapped pool over the host link);
+ *   5. emit the fixed-shape slot tensor and the per-(b,l) hit and miss counts
+ *      (hits_dev / misses_dev [B][L] int32).
+ * The hot row of (request r, layer l, slot s) is at
+ * skv_hot_buffer() + ((r*L + l)*S + s) * row_bytes.
+ * Inputs and outputs are device memory, B <= max_batch.  B == 0 enqueues
+ * nothing and does not advance the clock.  Captures into a CUDA graph. */
+SKV_API skv_status skv_assemble(skv_ctx *ctx, const int32_t *req_ids_dev, int32_t B, const int32_t *topk_dev,
+                        int32_t *slots_dev, int32_t *hits_dev, int32_t *misses_dev, skv_stream_t stream);
+
+/* skv_assemble for callers whose per-step tensors live in host memory
+ * (pinned or pageable): copies req_ids [B] and topk [B][L][k] to device
+ * staging buffers owned by the context, runs skv_assemble, copies slots, hits
+ * and misses back, and synchronises `stream`.  Same semantics and errors. */
+SKV_API skv_status skv_assemble_host(skv_ctx *ctx, const int32_t *req_ids, int32_t B, const int32_t *topk, int32_t *slots,
+                             int32_t *hits, int32_t *misses, skv_stream_t stream);
+
+/* Release a request (lifecycle step "release"): its slot becomes free, its
+ * maps are reset and its hot rows zeroed (enqueued on `stream`).  A later
+ * skv_publish may hand the same id out again.  SKV_ERR_BAD_REQUEST if req is
+ * not an active request. */
+SKV_API skv_status skv_release(skv_ctx *ctx, int32_t req, skv_stream_t stream);
+
+/* Read the sticky device error word into *bits (SKV_DEVERR_* mask, 0 = none)
+ * and clear it.  Synchronises `stream`. */
+SKV_API skv_status skv_get_device_error(skv_ctx *ctx, int32_t *bits, skv_stream_t stream);
+
+/* Device address of the hot buffer and the bytes between consecutive
+ * (request, layer) units (S * row_bytes).  Either pointer may be null. */
+SKV_API skv_status skv_hot_buffer(skv_ctx *ctx, void **base, int64_t *unit_stride_bytes);
+
+/* Host address of the pool; row (r, l, t) is at
+ * base + ((r*L + l)*T_max + t) * row_bytes.  The same memory is mapped for
+ * the device.  The caller may write rows [0, T) of a request it has just
+ * published with rows == null, before the first skv_assemble on it. */
+SKV_API skv_status skv_pool_rows(skv_ctx *ctx, void **host_base);
+
+/* Debug / parity: copy one request's state to host memory after synchronising
+ * `stream`.  Any output pointer may be null.  slot2tok, ts, lru are [L][S]
+ * (lru as int32 slot ids, least recently used first), tok2slot is
+ * [L][T_max], *len the request's token count, *active 1 or 0. */
+SKV_API skv_status skv_export_state(skv_ctx *ctx, int32_t req, int32_t *slot2tok, uint32_t *ts, int32_t *tok2slot,
+                            int32_t *lru, int64_t *len, int32_t *active, skv_stream_t stream);
+
+/* Debug / parity: copy one request's hot rows [L][S][row_bytes] to host
+ * memory after synchronising `stream`. */
+SKV_API skv_status skv_export_hot(skv_ctx *ctx, int32_t req, void *host_dst, skv_stream_t stream);
+
+/* The step clock (number of successful skv_assemble calls), after
+ * synchronising `stream`. */
+SKV_API skv_status skv_get_clock(skv_ctx *ctx, uint32_t *clock, skv_stream_t stream);
+
+/* Running totals since create, after synchronising `stream`: successful
+ * assemble calls, hit entries and missed (gathered) rows. */
+SKV_API skv_status skv_get_stats(skv_ctx *ctx, uint64_t *calls, uint64_t *hits, uint64_t *misses, skv_stream_t stream);
+
+/* Optional timing hooks: when set (non-null), skv_assemble records `before`
+ * just before its gather kernel and `after` just after it on the call's
+ * stream (external event records, so they also work inside a captured
+ * graph).  Pass two nulls to clear; passing exactly one null is
+ * SKV_ERR_INVALID_ARG.  The events belong to the caller. */
+SKV_API skv_status skv_set_gather_events(skv_ctx *ctx, skv_event_t before, skv_event_t after);
+
+/* The message of the last failing CUDA call on this thread ("" if none). */
+SKV_API const char *skv_last_cuda_error(void);
+
+/* Human-readable name of a status. */
+SKV_API const char *skv_status_string(skv_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SKV_H_ */

@@ -1,0 +1,416 @@
+// Host runtime behind the C ABI (include/skv.h): context creation and memory
+// layout, the request table, argument checks, and the stream-ordered launch
+// sequences of each call.  No call after skv_create allocates memory.
+//
+// Pages: the SparseKVCacheManager consists of host storage, a device cache and
+// an index mapping ("Sparse Attention-Driven KVCache Management for Domestic
+// AI Supernodes", agenda item 2); requests go through publish, acquire, write
+// back and release ("XM-Sparse: Netpreme X-Mem ...", section on the SGLang
+// HiSparse integration).
+
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <string>
+#include <thread>
+#include <vector>
+
+#include "skv.h"
+#include "skv_internal.cuh"
+
+using skv::Dev;
+
+struct skv_ctx {
+    skv_config cfg{};
+    Dev d{};
+    uint8_t* pool_host = nullptr;  // same memory as d.pool (mapped)
+    std::vector<uint8_t> active_h;  // host mirror of the request table
+    int32_t* st_req = nullptr;      // staging for skv_assemble_host
+    int32_t* st_topk = nullptr;
+    int32_t* st_slots = nullptr;
+    int32_t* st_hits = nullptr;
+    int32_t* st_misses = nullptr;
+    uint32_t* host_word = nullptr;  // pinned word for reading the error bits
+    cudaEvent_t ev_before = nullptr, ev_after = nullptr;
+    int gather_grid = 0;
+};
+
+namespace {
+
+thread_local std::string g_last_cuda_error;
+
+skv_status cuda_fail(cudaError_t e, const char* what)
+{
+    g_last_cuda_error = std::string(what) + ": " + cudaGetErrorString(e);
+    return SKV_ERR_CUDA;
+}
+
+#define SKV_CUDA(call)                                       \
+    do {                                                     \
+        cudaError_t e_ = (call);                             \
+        if (e_ != cudaSuccess) return cuda_fail(e_, #call);  \
+    } while (0)
+
+// Makes the context's device current for the duration of a call.
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = true;
+    explicit DeviceGuard(int dev)
+    {
+        if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+        if (prev != dev) ok = cudaSetDevice(dev) == cudaSuccess;
+    }
+    ~DeviceGuard()
+    {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+bool is_device_pointer(const void* p)
+{
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+void free_ctx(skv_ctx* c)
+{
+    if (!c) return;
+    cudaFree(c->d.tok2slot);
+    cudaFree(c->d.slot2tok);
+    cudaFree(c->d.ts);
+    cudaFree(c->d.lru);
+    cudaFree(c->d.hot);
+    cudaFree(c->d.len);
+    cudaFree(c->d.active);
+    cudaFree(c->d.ctl);
+    cudaFree(c->d.stats);
+    cudaFree(c->d.jobs);
+    cudaFree(c->d.wb_pos);
+    cudaFree(c->st_req);
+    cudaFree(c->st_topk);
+    cudaFree(c->st_slots);
+    cudaFree(c->st_hits);
+    cudaFree(c->st_misses);
+    if (c->host_word) cudaFreeHost(c->host_word);
+    if (c->pool_host) cudaFreeHost(c->pool_host);
+    delete c;
+}
+
+// Parallel host memcpy for large publishes from host memory.
+void host_copy(uint8_t* dst, const uint8_t* src, size_t n)
+{
+    const size_t chunk = (size_t)64 << 20;
+    if (n <= chunk) {
+        std::memcpy(dst, src, n);
+        return;
+    }
+    unsigned nt = std::thread::hardware_concurrency();
+    nt = nt < 1 ? 1 : (nt > 16 ? 16 : nt);
+    std::vector<std::thread> th;
+    const size_t per = (n + nt - 1) / nt;
+    for (unsigned i = 0; i < nt; ++i) {
+        const size_t o = (size_t)i * per;
+        if (o >= n) break;
+        const size_t len = n - o < per ? n - o : per;
+        th.emplace_back([=] { std::memcpy(dst + o, src + o, len); });
+    }
+    for (auto& t : th) t.join();
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* skv_last_cuda_error(void) { return g_last_cuda_error.c_str(); }
+
+const char* skv_status_string(skv_status s)
+{
+    switch (s) {
+        case SKV_OK: return "SKV_OK";
+        case SKV_ERR_INVALID_ARG: return "SKV_ERR_INVALID_ARG";
+        case SKV_ERR_OOM: return "SKV_ERR_OOM";
+        case SKV_ERR_BAD_REQUEST: return "SKV_ERR_BAD_REQUEST";
+        case SKV_ERR_NO_FREE_REQUEST: return "SKV_ERR_NO_FREE_REQUEST";
+        case SKV_ERR_CONTEXT_FULL: return "SKV_ERR_CONTEXT_FULL";
+        case SKV_ERR_CUDA: return "SKV_ERR_CUDA";
+    }
+    return "unknown skv_status";
+}
+
+skv_status skv_create(const skv_config* cfg, skv_ctx** out)
+{
+    if (!cfg || !out) return SKV_ERR_INVALID_ARG;
+    *out = nullptr;
+    const skv_config c = *cfg;
+    if (c.max_requests < 1 || c.num_layers < 1 || c.max_context < 1 || c.row_bytes < 16 || c.row_bytes % 16 != 0 ||
+        c.topk < 1 || c.topk > skv::kMaxTopk || c.hot_slots < c.topk || c.hot_slots > skv::kMaxSlots ||
+        c.max_batch < 1 || c.device < 0)
+        return SKV_ERR_INVALID_ARG;
+    const uint64_t units = (uint64_t)c.max_requests * (uint64_t)c.num_layers;
+    if (units * (uint64_t)c.max_context >= (1ull << 32) || units * (uint64_t)c.hot_slots >= (1ull << 32))
+        return SKV_ERR_INVALID_ARG;
+    if ((uint64_t)c.max_batch * c.num_layers * c.topk >= (1ull << 31) || (uint64_t)c.max_batch * c.num_layers >= (1ull << 31))
+        return SKV_ERR_INVALID_ARG;
+
+    DeviceGuard g(c.device);
+    if (!g.ok) return cuda_fail(cudaGetLastError(), "cudaSetDevice");
+    skv_ctx* x = new (std::nothrow) skv_ctx();
+    if (!x) return SKV_ERR_OOM;
+    x->cfg = c;
+    x->active_h.assign(c.max_requests, 0);
+    Dev& d = x->d;
+    d.R = c.max_requests;
+    d.L = c.num_layers;
+    d.k = c.topk;
+    d.S = c.hot_slots;
+    d.row_bytes = c.row_bytes;
+    d.T_max = c.max_context;
+
+    auto fail = [&](cudaError_t e, const char* what) {
+        skv_status s = (e == cudaErrorMemoryAllocation) ? SKV_ERR_OOM : cuda_fail(e, what);
+        if (e == cudaErrorMemoryAllocation) g_last_cuda_error = std::string(what) + ": out of memory";
+        cudaGetLastError();
+        free_ctx(x);
+        return s;
+    };
+#define SKV_TRY(call)                                \
+    do {                                             \
+        cudaError_t e_ = (call);                     \
+        if (e_ != cudaSuccess) return fail(e_, #call); \
+    } while (0)
+
+    const size_t pool_bytes = (size_t)units * c.max_context * c.row_bytes;
+    SKV_TRY(cudaHostAlloc((void**)&x->pool_host, pool_bytes, cudaHostAllocMapped | cudaHostAllocPortable));
+    SKV_TRY(cudaHostGetDevicePointer((void**)&d.pool, x->pool_host, 0));
+    SKV_TRY(cudaHostAlloc((void**)&x->host_word, 64, cudaHostAllocDefault));
+    SKV_TRY(cudaMalloc(&d.tok2slot, (size_t)units * c.max_context * 4));
+    SKV_TRY(cudaMalloc(&d.slot2tok, (size_t)units * c.hot_slots * 4));
+    SKV_TRY(cudaMalloc(&d.ts, (size_t)units * c.hot_slots * 4));
+    SKV_TRY(cudaMalloc(&d.lru, (size_t)units * c.hot_slots * 2));
+    SKV_TRY(cudaMalloc(&d.hot, (size_t)units * c.hot_slots * c.row_bytes));
+    SKV_TRY(cudaMalloc(&d.len, (size_t)c.max_requests * 8));
+    SKV_TRY(cudaMalloc(&d.active, (size_t)c.max_requests * 4));
+    SKV_TRY(cudaMalloc(&d.ctl, skv::CTL_WORDS * 4));
+    SKV_TRY(cudaMalloc(&d.stats, skv::STAT_WORDS * 8));
+    const size_t step_entries = (size_t)c.max_batch * c.num_layers * c.topk;
+    SKV_TRY(cudaMalloc(&d.jobs, step_entries * sizeof(uint2)));
+    SKV_TRY(cudaMalloc(&d.wb_pos, (size_t)c.max_batch * 8));
+    SKV_TRY(cudaMalloc(&x->st_req, (size_t)c.max_batch * 4));
+    SKV_TRY(cudaMalloc(&x->st_topk, step_entries * 4));
+    SKV_TRY(cudaMalloc(&x->st_slots, step_entries * 4));
+    SKV_TRY(cudaMalloc(&x->st_hits, (size_t)c.max_batch * c.num_layers * 4));
+    SKV_TRY(cudaMalloc(&x->st_misses, (size_t)c.max_batch * c.num_layers * 4));
+
+    SKV_TRY(cudaMemset(d.tok2slot, 0xFF, (size_t)units * c.max_context * 4));
+    SKV_TRY(cudaMemset(d.slot2tok, 0xFF, (size_t)units * c.hot_slots * 4));
+    SKV_TRY(cudaMemset(d.ts, 0, (size_t)units * c.hot_slots * 4));
+    SKV_TRY(cudaMemset(d.hot, 0, (size_t)units * c.hot_slots * c.row_bytes));
+    SKV_TRY(cudaMemset(d.len, 0, (size_t)c.max_requests * 8));
+    SKV_TRY(cudaMemset(d.active, 0, (size_t)c.max_requests * 4));
+    SKV_TRY(cudaMemset(d.ctl, 0, skv::CTL_WORDS * 4));
+    SKV_TRY(cudaMemset(d.stats, 0, skv::STAT_WORDS * 8));
+    SKV_TRY(skv::launch_init_lru_all(d, 0));
+    SKV_TRY(skv::prepare_step_kernels(c.topk, c.hot_slots, &x->gather_grid));
+    SKV_TRY(cudaDeviceSynchronize());
+#undef SKV_TRY
+    *out = x;
+    return SKV_OK;
+}
+
+skv_status skv_destroy(skv_ctx* ctx)
+{
+    if (!ctx) return SKV_OK;
+    DeviceGuard g(ctx->cfg.device);
+    cudaDeviceSynchronize();
+    free_ctx(ctx);
+    return SKV_OK;
+}
+
+skv_status skv_publish(skv_ctx* ctx, const void* rows, int64_t T, int32_t* out_req, skv_stream_t stream)
+{
+    if (!ctx || !out_req || T < 0) return SKV_ERR_INVALID_ARG;
+    if (T > ctx->cfg.max_context) return SKV_ERR_CONTEXT_FULL;
+    int32_t r = -1;
+    for (int32_t i = 0; i < ctx->cfg.max_requests; ++i)
+        if (!ctx->active_h[i]) {
+            r = i;
+            break;
+        }
+    if (r < 0) return SKV_ERR_NO_FREE_REQUEST;
+    DeviceGuard g(ctx->cfg.device);
+    const Dev& d = ctx->d;
+    const size_t rb = (size_t)d.row_bytes;
+    if (rows && T > 0) {
+        if (is_device_pointer(rows)) {
+            for (int l = 0; l < d.L; ++l)
+                SKV_CUDA(cudaMemcpyAsync(ctx->pool_host + (((size_t)r * d.L + l) * d.T_max) * rb,
+                                         static_cast<const uint8_t*>(rows) + (size_t)l * T * rb, (size_t)T * rb,
+                                         cudaMemcpyDefault, stream));
+        } else {
+            SKV_CUDA(cudaStreamSynchronize(stream));
+            for (int l = 0; l < d.L; ++l)
+                host_copy(ctx->pool_host + (((size_t)r * d.L + l) * d.T_max) * rb,
+                          static_cast<const uint8_t*>(rows) + (size_t)l * T * rb, (size_t)T * rb);
+        }
+    }
+    SKV_CUDA(skv::launch_reset_request(d, r, T, 1, stream));
+    ctx->active_h[r] = 1;
+    *out_req = r;
+    return SKV_OK;
+}
+
+skv_status skv_release(skv_ctx* ctx, int32_t req, skv_stream_t stream)
+{
+    if (!ctx) return SKV_ERR_INVALID_ARG;
+    if (req < 0 || req >= ctx->cfg.max_requests || !ctx->active_h[req]) return SKV_ERR_BAD_REQUEST;
+    DeviceGuard g(ctx->cfg.device);
+    SKV_CUDA(skv::launch_reset_request(ctx->d, req, 0, 0, stream));
+    ctx->active_h[req] = 0;
+    return SKV_OK;
+}
+
+skv_status skv_write_back(skv_ctx* ctx, const int32_t* req_ids_dev, int32_t n, const void* rows_dev,
+                          skv_stream_t stream)
+{
+    if (!ctx || n < 0 || n > ctx->cfg.max_batch) return SKV_ERR_INVALID_ARG;
+    if (n == 0) return SKV_OK;
+    if (!req_ids_dev || !rows_dev || (reinterpret_cast<uintptr_t>(rows_dev) & 15u)) return SKV_ERR_INVALID_ARG;
+    DeviceGuard g(ctx->cfg.device);
+    SKV_CUDA(skv::launch_write_back(ctx->d, req_ids_dev, n, rows_dev, stream));
+    return SKV_OK;
+}
+
+skv_status skv_assemble(skv_ctx* ctx, const int32_t* req_ids_dev, int32_t B, const int32_t* topk_dev,
+                        int32_t* slots_dev, int32_t* hits_dev, int32_t* misses_dev, skv_stream_t stream)
+{
+    if (!ctx || B < 0 || B > ctx->cfg.max_batch) return SKV_ERR_INVALID_ARG;
+    if (B == 0) return SKV_OK;
+    if (!req_ids_dev || !topk_dev || !slots_dev || !hits_dev || !misses_dev) return SKV_ERR_INVALID_ARG;
+    DeviceGuard g(ctx->cfg.device);
+    const Dev& d = ctx->d;
+    SKV_CUDA(skv::launch_validate(d, req_ids_dev, B, topk_dev, stream));
+    SKV_CUDA(skv::launch_plan(d, req_ids_dev, B, topk_dev, slots_dev, hits_dev, misses_dev, stream));
+    if (ctx->ev_before) SKV_CUDA(cudaEventRecordWithFlags(ctx->ev_before, stream, cudaEventRecordExternal));
+    SKV_CUDA(skv::launch_gather(d, ctx->gather_grid, stream));
+    if (ctx->ev_after) SKV_CUDA(cudaEventRecordWithFlags(ctx->ev_after, stream, cudaEventRecordExternal));
+    return SKV_OK;
+}
+
+skv_status skv_assemble_host(skv_ctx* ctx, const int32_t* req_ids, int32_t B, const int32_t* topk, int32_t* slots,
+                             int32_t* hits, int32_t* misses, skv_stream_t stream)
+{
+    if (!ctx || B < 0 || B > ctx->cfg.max_batch) return SKV_ERR_INVALID_ARG;
+    if (B == 0) return SKV_OK;
+    if (!req_ids || !topk || !slots || !hits || !misses) return SKV_ERR_INVALID_ARG;
+    DeviceGuard g(ctx->cfg.device);
+    const size_t units = (size_t)B * ctx->cfg.num_layers;
+    const size_t entries = units * ctx->cfg.topk;
+    SKV_CUDA(cudaMemcpyAsync(ctx->st_req, req_ids, (size_t)B * 4, cudaMemcpyHostToDevice, stream));
+    SKV_CUDA(cudaMemcpyAsync(ctx->st_topk, topk, entries * 4, cudaMemcpyHostToDevice, stream));
+    skv_status s = skv_assemble(ctx, ctx->st_req, B, ctx->st_topk, ctx->st_slots, ctx->st_hits, ctx->st_misses, stream);
+    if (s != SKV_OK) return s;
+    SKV_CUDA(cudaMemcpyAsync(slots, ctx->st_slots, entries * 4, cudaMemcpyDeviceToHost, stream));
+    SKV_CUDA(cudaMemcpyAsync(hits, ctx->st_hits, units * 4, cudaMemcpyDeviceToHost, stream));
+    SKV_CUDA(cudaMemcpyAsync(misses, ctx->st_misses, units * 4, cudaMemcpyDeviceToHost, stream));
+    SKV_CUDA(cudaStreamSynchronize(stream));
+    return SKV_OK;
+}
+
+skv_status skv_get_device_error(skv_ctx* ctx, int32_t* bits, skv_stream_t stream)
+{
+    if (!ctx || !bits) return SKV_ERR_INVALID_ARG;
+    DeviceGuard g(ctx->cfg.device);
+    SKV_CUDA(cudaMemcpyAsync(ctx->host_word, ctx->d.ctl + skv::CTL_ERR, 4, cudaMemcpyDeviceToHost, stream));
+    SKV_CUDA(cudaMemsetAsync(ctx->d.ctl + skv::CTL_ERR, 0, 4, stream));
+    SKV_CUDA(cudaStreamSynchronize(stream));
+    *bits = (int32_t)ctx->host_word[0];
+    return SKV_OK;
+}
+
+skv_status skv_hot_buffer(skv_ctx* ctx, void** base, int64_t* unit_stride_bytes)
+{
+    if (!ctx) return SKV_ERR_INVALID_ARG;
+    if (base) *base = ctx->d.hot;
+    if (unit_stride_bytes) *unit_stride_bytes = (int64_t)ctx->d.S * ctx->d.row_bytes;
+    return SKV_OK;
+}
+
+skv_status skv_pool_rows(skv_ctx* ctx, void** host_base)
+{
+    if (!ctx || !host_base) return SKV_ERR_INVALID_ARG;
+    *host_base = ctx->pool_host;
+    return SKV_OK;
+}
+
+skv_status skv_export_state(skv_ctx* ctx, int32_t req, int32_t* slot2tok, uint32_t* ts, int32_t* tok2slot,
+                            int32_t* lru, int64_t* len, int32_t* active, skv_stream_t stream)
+{
+    if (!ctx) return SKV_ERR_INVALID_ARG;
+    if (req < 0 || req >= ctx->cfg.max_requests) return SKV_ERR_BAD_REQUEST;
+    DeviceGuard g(ctx->cfg.device);
+    const Dev& d = ctx->d;
+    const size_t u0 = (size_t)req * d.L;
+    const size_t ns = (size_t)d.L * d.S;
+    SKV_CUDA(cudaStreamSynchronize(stream));
+    if (slot2tok) SKV_CUDA(cudaMemcpy(slot2tok, d.slot2tok + u0 * d.S, ns * 4, cudaMemcpyDeviceToHost));
+    if (ts) SKV_CUDA(cudaMemcpy(ts, d.ts + u0 * d.S, ns * 4, cudaMemcpyDeviceToHost));
+    if (tok2slot) SKV_CUDA(cudaMemcpy(tok2slot, d.tok2slot + u0 * d.T_max, (size_t)d.L * d.T_max * 4,
+                                      cudaMemcpyDeviceToHost));
+    if (lru) {
+        std::vector<uint16_t> tmp(ns);
+        SKV_CUDA(cudaMemcpy(tmp.data(), d.lru + u0 * d.S, ns * 2, cudaMemcpyDeviceToHost));
+        for (size_t i = 0; i < ns; ++i) lru[i] = tmp[i];
+    }
+    if (len) SKV_CUDA(cudaMemcpy(len, d.len + req, 8, cudaMemcpyDeviceToHost));
+    if (active) SKV_CUDA(cudaMemcpy(active, d.active + req, 4, cudaMemcpyDeviceToHost));
+    return SKV_OK;
+}
+
+skv_status skv_export_hot(skv_ctx* ctx, int32_t req, void* host_dst, skv_stream_t stream)
+{
+    if (!ctx || !host_dst) return SKV_ERR_INVALID_ARG;
+    if (req < 0 || req >= ctx->cfg.max_requests) return SKV_ERR_BAD_REQUEST;
+    DeviceGuard g(ctx->cfg.device);
+    const Dev& d = ctx->d;
+    SKV_CUDA(cudaStreamSynchronize(stream));
+    SKV_CUDA(cudaMemcpy(host_dst, d.hot + (size_t)req * d.L * d.S * d.row_bytes, (size_t)d.L * d.S * d.row_bytes,
+                        cudaMemcpyDeviceToHost));
+    return SKV_OK;
+}
+
+skv_status skv_get_clock(skv_ctx* ctx, uint32_t* clock, skv_stream_t stream)
+{
+    if (!ctx || !clock) return SKV_ERR_INVALID_ARG;
+    DeviceGuard g(ctx->cfg.device);
+    SKV_CUDA(cudaStreamSynchronize(stream));
+    SKV_CUDA(cudaMemcpy(clock, ctx->d.ctl + skv::CTL_CLOCK, 4, cudaMemcpyDeviceToHost));
+    return SKV_OK;
+}
+
+skv_status skv_get_stats(skv_ctx* ctx, uint64_t* calls, uint64_t* hits, uint64_t* misses, skv_stream_t stream)
+{
+    if (!ctx) return SKV_ERR_INVALID_ARG;
+    DeviceGuard g(ctx->cfg.device);
+    unsigned long long st[skv::STAT_WORDS];
+    SKV_CUDA(cudaStreamSynchronize(stream));
+    SKV_CUDA(cudaMemcpy(st, ctx->d.stats, sizeof(st), cudaMemcpyDeviceToHost));
+    if (calls) *calls = st[skv::STAT_CALLS];
+    if (hits) *hits = st[skv::STAT_HITS];
+    if (misses) *misses = st[skv::STAT_MISSES];
+    return SKV_OK;
+}
+
+skv_status skv_set_gather_events(skv_ctx* ctx, skv_event_t before, skv_event_t after)
+{
+    if (!ctx || (before == nullptr) != (after == nullptr)) return SKV_ERR_INVALID_ARG;
+    ctx->ev_before = reinterpret_cast<cudaEvent_t>(before);
+    ctx->ev_after = reinterpret_cast<cudaEvent_t>(after);
+    return SKV_OK;
+}
+
+}  // extern "C"

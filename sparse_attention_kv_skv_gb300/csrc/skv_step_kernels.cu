@@ -1,0 +1,456 @@
+// Kernels of one assemble step: validate -> plan (sparse diff + LRU slot
+// allocation + map update + slot emission) -> gather (host pool -> HBM).
+//
+// Pages: per-step, Top-k-driven token-level assembly into a device cache
+// ("Sparse Attention-Driven KVCache Management for Domestic AI Supernodes",
+// abstract and agenda item 2); the Sparse Diff Kernel moves only the
+// difference against the resident set, and the GPU keeps a Top-k LRU buffer
+// ("SGLang и Tair представили иерархичную Sparse Attention ...", paragraphs 1
+// and 3); the whole step stays graph-executable ("XM-Sparse: Netpreme X-Mem
+// ...", section on the SGLang HiSparse integration).
+//
+// All three kernels have fixed launch shapes that depend only on (B, L, k, S)
+// and the device, and read the data-dependent sizes (miss counts, error bits)
+// from device memory, so the step can be captured in a CUDA graph.
+
+#include "skv_internal.cuh"
+
+namespace skv {
+namespace {
+
+constexpr uint32_t kEmpty = 0xFFFFFFFFu;
+constexpr int kMaxIpt = kMaxTopk / kPlanThreads;  // Top-k entries per plan thread
+
+// ---------------------------------------------------------------------------
+// block-wide exclusive prefix sum (blockDim.x a multiple of 32, <= 1024);
+// `sh` is >= 32 words of shared memory; all threads must call it.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* total, uint32_t* sh)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    uint32_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        uint32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) sh[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t w = lane < nw ? sh[lane] : 0u;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            uint32_t y = __shfl_up_sync(0xFFFFFFFFu, w, o);
+            if (lane >= o) w += y;
+        }
+        if (lane < nw) sh[lane] = w;
+    }
+    __syncthreads();
+    const uint32_t before = warp > 0 ? sh[warp - 1] : 0u;
+    *total = sh[nw - 1];
+    __syncthreads();
+    return before + x - v;
+}
+
+__device__ __forceinline__ bool bit_test(const uint32_t* bm, int s) { return (bm[s >> 5] >> (s & 31)) & 1u; }
+
+// ---------------------------------------------------------------------------
+// validate: one CTA per (b, l).  Checks the request id (in range, active, not
+// repeated in the batch -- the l == 0 CTA of each b compares with the earlier
+// entries) and every Top-k entry (-1 or in [0, len)), and finds repeated
+// tokens with an open-addressing set in shared memory.  Error bits go to
+// CTL_ERR_CALL; nothing else is written except the reset of the gather list.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kValidateThreads) validate_kernel(Dev d, const int32_t* __restrict__ req_ids, int B,
+                                                                    const int32_t* __restrict__ topk, int table_log2)
+{
+    extern __shared__ uint32_t table[];
+    __shared__ uint32_t flags;
+    if (blockIdx.x == 0 && threadIdx.x == 0) d.ctl[CTL_JOBS] = 0;
+    if (d.ctl[CTL_ERR] != 0) return;  // sticky error: the call is a no-op
+    const int b = blockIdx.x / d.L, l = blockIdx.x % d.L;
+    const int32_t r = req_ids[b];
+    if (r < 0 || r >= d.R || d.active[r] == 0) {
+        if (threadIdx.x == 0) atomicOr(&d.ctl[CTL_ERR_CALL], DEVERR_BAD_REQUEST);
+        return;  // uniform across the CTA
+    }
+    uint32_t f = 0;
+    if (l == 0)
+        for (int j = threadIdx.x; j < b; j += blockDim.x)
+            if (req_ids[j] == r) f |= DEVERR_BAD_REQUEST;
+    const int H = 1 << table_log2;
+    for (int j = threadIdx.x; j < H; j += blockDim.x) table[j] = kEmpty;
+    if (threadIdx.x == 0) flags = 0;
+    __syncthreads();
+    const int64_t len = d.len[r];
+    const int32_t* row = topk + (size_t)blockIdx.x * d.k;
+    for (int i = threadIdx.x; i < d.k; i += blockDim.x) {
+        const int32_t t = row[i];
+        if (t == -1) continue;
+        if (t < 0 || (int64_t)t >= len) {
+            f |= DEVERR_BAD_INDEX;
+            continue;
+        }
+        uint32_t h = ((uint32_t)t * 2654435761u) >> (32 - table_log2);
+        // H >= 2k, so an empty cell is always reachable: at most H probes
+        for (int probe = 0; probe < H; ++probe) {
+            const uint32_t prev = atomicCAS(&table[h], kEmpty, (uint32_t)t);
+            if (prev == kEmpty) break;
+            if (prev == (uint32_t)t) {
+                f |= DEVERR_DUPLICATE;
+                break;
+            }
+            h = (h + 1) & (uint32_t)(H - 1);
+        }
+    }
+    if (f) atomicOr(&flags, f);
+    __syncthreads();
+    if (threadIdx.x == 0 && flags) atomicOr(&d.ctl[CTL_ERR_CALL], flags);
+}
+
+// ---------------------------------------------------------------------------
+// plan: one CTA of kPlanThreads per (b, l).
+//   A. sparse diff: probe tok2slot for every entry (blocked arrangement, so a
+//      block-wide scan keeps row order); hits mark a bitmap over the slots and
+//      are stamped with the new clock; misses are compacted.
+//   B. misses are ordered by token (already ordered when the row is sorted;
+//      otherwise a bitonic sort in shared memory).
+//   C. LRU allocation: walking the unit's LRU order, the first m non-hit
+//      slots are the victims, paired in order with the ascending misses.
+//   D. new LRU order: untouched slots keep their order, then the slots the
+//      step used, by slot index.
+//   E. map update per miss (evicted token leaves tok2slot), slot emission,
+//      and a gather job (pool row -> hot row).
+// ---------------------------------------------------------------------------
+struct PlanSmem {
+    uint32_t* hitbits;    // [SW]
+    uint32_t* vicbits;    // [SW]
+    int32_t* out;         // [k]
+    unsigned long long* miss;  // [P] (token << 32 | row position)
+    uint16_t* victim;     // [k]
+    uint16_t* lru_old;    // [S]
+    uint16_t* lru_new;    // [S]
+};
+
+__host__ __device__ inline int next_pow2(int x)
+{
+    int p = 1;
+    while (p < x) p <<= 1;
+    return p;
+}
+
+__host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~(size_t)15; }
+
+__device__ inline PlanSmem carve_plan_smem(uint8_t* base, int k, int S)
+{
+    PlanSmem m;
+    const int SW = (S + 31) / 32;
+    size_t o = 0;
+    m.miss = (unsigned long long*)(base + o); o += align16((size_t)next_pow2(k) * 8);
+    m.hitbits = (uint32_t*)(base + o); o += align16((size_t)SW * 4);
+    m.vicbits = (uint32_t*)(base + o); o += align16((size_t)SW * 4);
+    m.out = (int32_t*)(base + o); o += align16((size_t)k * 4);
+    m.victim = (uint16_t*)(base + o); o += align16((size_t)k * 2);
+    m.lru_old = (uint16_t*)(base + o); o += align16((size_t)S * 2);
+    m.lru_new = (uint16_t*)(base + o);
+    return m;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(Dev d, const int32_t* __restrict__ req_ids,
+                                                            const int32_t* __restrict__ topk,
+                                                            int32_t* __restrict__ slots_out,
+                                                            int32_t* __restrict__ hits_out,
+                                                            int32_t* __restrict__ misses_out)
+{
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    __shared__ uint32_t scan_sh[32];
+    __shared__ uint32_t job_base_sh;
+    const int tid = threadIdx.x, NT = blockDim.x;
+    const int k = d.k, S = d.S;
+    const int32_t* row = topk + (size_t)blockIdx.x * k;
+    int32_t* out = slots_out + (size_t)blockIdx.x * k;
+
+    if ((d.ctl[CTL_ERR] | d.ctl[CTL_ERR_CALL]) != 0) {  // rejected call: -1 outputs, no state change
+        for (int i = tid; i < k; i += NT) out[i] = -1;
+        if (tid == 0) {
+            hits_out[blockIdx.x] = -1;
+            misses_out[blockIdx.x] = -1;
+        }
+        return;
+    }
+
+    PlanSmem sm = carve_plan_smem(smem_raw, k, S);
+    const int b = blockIdx.x / d.L, l = blockIdx.x % d.L;
+    const int64_t u = (int64_t)req_ids[b] * d.L + l;
+    int32_t* t2s = d.tok2slot + u * d.T_max;
+    int32_t* s2t = d.slot2tok + u * S;
+    uint32_t* tsu = d.ts + u * S;
+    uint16_t* lru = d.lru + u * S;
+    const uint32_t now1 = d.ctl[CTL_CLOCK] + 1u;
+    const int SW = (S + 31) / 32;
+
+    for (int w = tid; w < SW; w += NT) {
+        sm.hitbits[w] = 0u;
+        sm.vicbits[w] = 0u;
+    }
+    for (int p = tid; p < S; p += NT) sm.lru_old[p] = lru[p];
+    __syncthreads();
+
+    // A. sparse diff
+    const int ipt = (k + NT - 1) / NT;
+    const int i0 = tid * ipt;
+    int32_t tok[kMaxIpt];
+    uint32_t missmask = 0, nmiss = 0, nhit = 0;
+#pragma unroll
+    for (int j = 0; j < kMaxIpt; ++j) {
+        const int i = i0 + j;
+        tok[j] = -1;
+        if (j < ipt && i < k) {
+            const int32_t t = row[i];
+            tok[j] = t;
+            if (t >= 0) {
+                const int32_t s = t2s[t];
+                if (s >= 0) {
+                    sm.out[i] = s;
+                    atomicOr(&sm.hitbits[s >> 5], 1u << (s & 31));
+                    tsu[s] = now1;
+                    ++nhit;
+                } else {
+                    missmask |= 1u << j;
+                    ++nmiss;
+                }
+            } else {
+                sm.out[i] = -1;
+            }
+        }
+    }
+    uint32_t total;
+    const uint32_t excl = block_excl_scan(nmiss | (nhit << 16), &total, scan_sh);
+    const int m = (int)(total & 0xFFFFu), h = (int)(total >> 16);
+    {
+        uint32_t o = excl & 0xFFFFu;
+#pragma unroll
+        for (int j = 0; j < kMaxIpt; ++j)
+            if (missmask & (1u << j))
+                sm.miss[o++] = ((unsigned long long)(uint32_t)tok[j] << 32) | (uint32_t)(i0 + j);
+    }
+    __syncthreads();
+
+    // B. misses in ascending token order
+    int unsorted = 0;
+    for (int j = tid; j + 1 < m; j += NT)
+        if ((sm.miss[j] >> 32) > (sm.miss[j + 1] >> 32)) unsorted = 1;
+    if (__syncthreads_or(unsorted)) {
+        const int P = next_pow2(m);
+        for (int j = m + tid; j < P; j += NT) sm.miss[j] = ~0ull;
+        __syncthreads();
+        for (int size = 2; size <= P; size <<= 1) {
+            for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                for (int i = tid; i < P / 2; i += NT) {
+                    const int lo = 2 * stride * (i / stride) + (i % stride), hi = lo + stride;
+                    const bool asc = (lo & size) == 0;
+                    const unsigned long long a = sm.miss[lo], c = sm.miss[hi];
+                    if ((a > c) == asc) {
+                        sm.miss[lo] = c;
+                        sm.miss[hi] = a;
+                    }
+                }
+                __syncthreads();
+            }
+        }
+    }
+
+    // C. victims: the first m non-hit slots in LRU order
+    const int spt = (S + NT - 1) / NT;
+    const int p0 = tid * spt;
+    uint32_t cnt = 0;
+    for (int j = 0; j < spt; ++j) {
+        const int p = p0 + j;
+        if (p < S && !bit_test(sm.hitbits, sm.lru_old[p])) ++cnt;
+    }
+    uint32_t tot2;
+    uint32_t rank = block_excl_scan(cnt, &tot2, scan_sh);
+    for (int j = 0; j < spt; ++j) {
+        const int p = p0 + j;
+        if (p >= S) break;
+        const int s = sm.lru_old[p];
+        if (bit_test(sm.hitbits, s)) continue;
+        if ((int)rank < m) {
+            sm.victim[rank] = (uint16_t)s;
+            atomicOr(&sm.vicbits[s >> 5], 1u << (s & 31));
+        } else {
+            sm.lru_new[rank - m] = (uint16_t)s;
+        }
+        ++rank;
+    }
+    __syncthreads();
+
+    // D. the slots used by this step go to the back, by slot index
+    const int untouched = S - h - m;
+    uint32_t cnt3 = 0;
+    for (int j = 0; j < spt; ++j) {
+        const int s = p0 + j;
+        if (s < S && (bit_test(sm.hitbits, s) || bit_test(sm.vicbits, s))) ++cnt3;
+    }
+    uint32_t tot3;
+    uint32_t pos = block_excl_scan(cnt3, &tot3, scan_sh);
+    for (int j = 0; j < spt; ++j) {
+        const int s = p0 + j;
+        if (s < S && (bit_test(sm.hitbits, s) || bit_test(sm.vicbits, s))) sm.lru_new[untouched + pos++] = (uint16_t)s;
+    }
+
+    // E. map update, slot emission, gather jobs
+    if (tid == 0) job_base_sh = m ? atomicAdd(&d.ctl[CTL_JOBS], (uint32_t)m) : 0u;
+    __syncthreads();
+    const uint32_t job_base = job_base_sh;
+    for (int j = tid; j < m; j += NT) {
+        const int v = sm.victim[j];
+        const unsigned long long key = sm.miss[j];
+        const int32_t t = (int32_t)(key >> 32);
+        const int i = (int)(key & 0xFFFFFFFFu);
+        const int32_t old = s2t[v];
+        if (old >= 0) t2s[old] = -1;
+        s2t[v] = t;
+        t2s[t] = v;
+        tsu[v] = now1;
+        sm.out[i] = v;
+        d.jobs[job_base + j] = make_uint2((uint32_t)(u * d.T_max + t), (uint32_t)(u * S + v));
+    }
+    __syncthreads();
+
+    for (int i = tid; i < k; i += NT) out[i] = sm.out[i];
+    for (int p = tid; p < S; p += NT) lru[p] = sm.lru_new[p];
+    if (tid == 0) {
+        hits_out[blockIdx.x] = h;
+        misses_out[blockIdx.x] = m;
+        if (h) atomicAdd(&d.stats[STAT_HITS], (unsigned long long)h);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// gather: copy every queued row (pool row -> hot row) in 16-byte chunks.
+// The chunk space (jobs x chunks per row) is walked grid-stride; each thread
+// issues U independent 16-byte loads from the mapped host pool before it
+// stores them, to keep many host-link reads in flight.  Block 0 also commits
+// the call: clock + 1 and statistics on success, error bits into the sticky
+// word.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int4 ld_stream(const int4* p)
+{
+    int4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.s32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+__device__ __forceinline__ void st_stream(int4* p, int4 v)
+{
+    asm volatile("st.global.cs.v4.s32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+template <int CPR_CONST, int U>
+__global__ void __launch_bounds__(kGatherThreads) gather_kernel(Dev d, int cpr_rt)
+{
+    const int cpr = CPR_CONST > 0 ? CPR_CONST : cpr_rt;  // 16-byte chunks per row
+    const uint32_t M = d.ctl[CTL_JOBS];
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        const uint32_t e = d.ctl[CTL_ERR_CALL];
+        if (d.ctl[CTL_ERR] == 0 && e == 0) {
+            d.ctl[CTL_CLOCK] += 1u;
+            d.stats[STAT_CALLS] += 1ull;
+            d.stats[STAT_MISSES] += (unsigned long long)M;
+        }
+        d.ctl[CTL_ERR] |= e;
+        d.ctl[CTL_ERR_CALL] = 0u;
+    }
+    const uint64_t total = (uint64_t)M * (uint64_t)cpr;
+    const int4* __restrict__ src = reinterpret_cast<const int4*>(d.pool);
+    int4* __restrict__ dst = reinterpret_cast<int4*>(d.hot);
+    const uint2* __restrict__ jobs = d.jobs;
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x * U;
+    for (uint64_t base = (uint64_t)blockIdx.x * blockDim.x * U + threadIdx.x; base < total; base += stride) {
+        int4 v[U];
+        uint64_t o[U];
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+            const uint64_t c = base + (uint64_t)j * blockDim.x;
+            if (c < total) {
+                const uint32_t job = (uint32_t)(c / (uint64_t)cpr);
+                const uint32_t w = (uint32_t)(c - (uint64_t)job * cpr);
+                const uint2 jb = jobs[job];
+                o[j] = (uint64_t)jb.y * cpr + w;
+                v[j] = ld_stream(src + (uint64_t)jb.x * cpr + w);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+            const uint64_t c = base + (uint64_t)j * blockDim.x;
+            if (c < total) st_stream(dst + o[j], v[j]);
+        }
+    }
+}
+
+constexpr int kGatherUnroll = 4;
+
+}  // namespace
+
+size_t plan_smem_bytes(int k, int S)
+{
+    const int SW = (S + 31) / 32;
+    return align16((size_t)next_pow2(k) * 8) + 2 * align16((size_t)SW * 4) + align16((size_t)k * 4) +
+           align16((size_t)k * 2) + 2 * align16((size_t)S * 2);
+}
+
+static int table_log2_for(int k)
+{
+    int lg = 1;
+    while ((1 << lg) < 2 * k) ++lg;
+    return lg;
+}
+
+size_t validate_smem_bytes(int k) { return ((size_t)1 << table_log2_for(k)) * 4; }
+
+cudaError_t prepare_step_kernels(int k, int S, int* gather_grid)
+{
+    cudaError_t e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)plan_smem_bytes(k, S));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(validate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)validate_smem_bytes(k));
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0, per_sm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_kernel<72, kGatherUnroll>,
+                                                           kGatherThreads, 0)) != cudaSuccess)
+        return e;
+    *gather_grid = sms * (per_sm > 0 ? per_sm : 1);
+    return cudaSuccess;
+}
+
+cudaError_t launch_validate(const Dev& d, const int32_t* req_ids, int B, const int32_t* topk, cudaStream_t st)
+{
+    const int lg = table_log2_for(d.k);
+    validate_kernel<<<B * d.L, kValidateThreads, validate_smem_bytes(d.k), st>>>(d, req_ids, B, topk, lg);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_plan(const Dev& d, const int32_t* req_ids, int B, const int32_t* topk, int32_t* slots,
+                        int32_t* hits, int32_t* misses, cudaStream_t st)
+{
+    plan_kernel<<<B * d.L, kPlanThreads, plan_smem_bytes(d.k, d.S), st>>>(d, req_ids, topk, slots, hits, misses);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const Dev& d, int grid, cudaStream_t st)
+{
+    const int cpr = d.row_bytes / 16;
+    if (cpr == 72)
+        gather_kernel<72, kGatherUnroll><<<grid, kGatherThreads, 0, st>>>(d, cpr);
+    else
+        gather_kernel<0, kGatherUnroll><<<grid, kGatherThreads, 0, st>>>(d, cpr);
+    return cudaGetLastError();
+}
+
+}  // namespace skv

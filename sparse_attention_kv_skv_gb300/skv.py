@@ -1,0 +1,254 @@
+"""Python binding of libskv.so (include/skv.h): argument marshalling only.
+
+Every function has the name of the C entry point it calls and passes plain
+integers (device or host addresses, sizes, CUDA stream handles) through
+ctypes.  No step of the path runs in Python, and there is no fallback: if the
+library is missing, importing this module raises.
+
+``Context`` is a convenience wrapper that takes torch tensors (it reads their
+``data_ptr()`` and torch's current CUDA stream) and raises ``SkvError`` for
+non-OK statuses.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libskv.so")
+
+SKV_OK = 0
+SKV_ERR_INVALID_ARG = 1
+SKV_ERR_OOM = 2
+SKV_ERR_BAD_REQUEST = 3
+SKV_ERR_NO_FREE_REQUEST = 4
+SKV_ERR_CONTEXT_FULL = 5
+SKV_ERR_CUDA = 6
+
+SKV_DEVERR_BAD_REQUEST = 1
+SKV_DEVERR_BAD_INDEX = 2
+SKV_DEVERR_DUPLICATE = 4
+SKV_DEVERR_CONTEXT_FULL = 8
+
+
+class skv_config(ctypes.Structure):
+    _fields_ = [
+        ("max_requests", ctypes.c_int32),
+        ("num_layers", ctypes.c_int32),
+        ("max_context", ctypes.c_int64),
+        ("row_bytes", ctypes.c_int32),
+        ("topk", ctypes.c_int32),
+        ("hot_slots", ctypes.c_int32),
+        ("max_batch", ctypes.c_int32),
+        ("device", ctypes.c_int32),
+    ]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with `python -m sparse_attention_kv_skv_gb300.build` "
+                          "(the CUDA library is required; there is no fallback)")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64, st = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_int
+    P = ctypes.POINTER
+    sigs = {
+        "skv_create": [P(skv_config), P(vp)],
+        "skv_destroy": [vp],
+        "skv_publish": [vp, vp, i64, P(i32), vp],
+        "skv_write_back": [vp, vp, i32, vp, vp],
+        "skv_assemble": [vp, vp, i32, vp, vp, vp, vp, vp],
+        "skv_assemble_host": [vp, vp, i32, vp, vp, vp, vp, vp],
+        "skv_release": [vp, i32, vp],
+        "skv_get_device_error": [vp, P(i32), vp],
+        "skv_hot_buffer": [vp, P(vp), P(i64)],
+        "skv_pool_rows": [vp, P(vp)],
+        "skv_export_state": [vp, i32, vp, vp, vp, vp, vp, vp, vp],
+        "skv_export_hot": [vp, i32, vp, vp],
+        "skv_get_clock": [vp, P(ctypes.c_uint32), vp],
+        "skv_get_stats": [vp, P(ctypes.c_uint64), P(ctypes.c_uint64), P(ctypes.c_uint64), vp],
+        "skv_set_gather_events": [vp, vp, vp],
+    }
+    for name, args in sigs.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = st
+    lib.skv_last_cuda_error.argtypes = []
+    lib.skv_last_cuda_error.restype = ctypes.c_char_p
+    lib.skv_status_string.argtypes = [st]
+    lib.skv_status_string.restype = ctypes.c_char_p
+    return lib
+
+
+lib = _load()
+
+# The C entry points under their own names (raw: they return the status).
+skv_create = lib.skv_create
+skv_destroy = lib.skv_destroy
+skv_publish = lib.skv_publish
+skv_write_back = lib.skv_write_back
+skv_assemble = lib.skv_assemble
+skv_assemble_host = lib.skv_assemble_host
+skv_release = lib.skv_release
+skv_get_device_error = lib.skv_get_device_error
+skv_hot_buffer = lib.skv_hot_buffer
+skv_pool_rows = lib.skv_pool_rows
+skv_export_state = lib.skv_export_state
+skv_export_hot = lib.skv_export_hot
+skv_get_clock = lib.skv_get_clock
+skv_get_stats = lib.skv_get_stats
+skv_set_gather_events = lib.skv_set_gather_events
+skv_last_cuda_error = lib.skv_last_cuda_error
+skv_status_string = lib.skv_status_string
+
+
+class SkvError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        msg = f"{what}: {skv_status_string(status).decode()}"
+        if status == SKV_ERR_CUDA:
+            msg += f" ({skv_last_cuda_error().decode()})"
+        super().__init__(msg)
+        self.status = status
+
+
+def check(status: int, what: str) -> None:
+    if status != SKV_OK:
+        raise SkvError(status, what)
+
+
+def _stream_handle(stream) -> int:
+    """A stream argument: None -> torch's current stream; an int -> as is;
+    a torch.cuda.Stream -> its handle."""
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _ptr(t) -> int:
+    if t is None:
+        return 0
+    if isinstance(t, int):
+        return t
+    if hasattr(t, "data_ptr"):
+        return t.data_ptr()
+    return t.ctypes.data  # numpy
+
+
+@dataclasses.dataclass
+class Config:
+    max_requests: int
+    num_layers: int
+    max_context: int
+    topk: int
+    hot_slots: int
+    max_batch: int
+    row_bytes: int = 1152
+    device: int = 0
+
+    def c(self) -> skv_config:
+        return skv_config(self.max_requests, self.num_layers, self.max_context, self.row_bytes, self.topk,
+                          self.hot_slots, self.max_batch, self.device)
+
+
+class Context:
+    """One library context (pool, hot buffer, maps) on one GPU."""
+
+    def __init__(self, cfg: Config):
+        self.cfg = cfg
+        h = ctypes.c_void_p()
+        c = cfg.c()
+        check(skv_create(ctypes.byref(c), ctypes.byref(h)), "skv_create")
+        self.h = h.value
+
+    def close(self):
+        if getattr(self, "h", None):
+            check(skv_destroy(self.h), "skv_destroy")
+            self.h = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # lifecycle -------------------------------------------------------------
+    def publish(self, T: int, rows=None, stream=None) -> int:
+        r = ctypes.c_int32()
+        check(skv_publish(self.h, _ptr(rows), T, ctypes.byref(r), _stream_handle(stream)), "skv_publish")
+        return r.value
+
+    def release(self, req: int, stream=None) -> None:
+        check(skv_release(self.h, req, _stream_handle(stream)), "skv_release")
+
+    def write_back(self, req_ids, rows, n: int | None = None, stream=None) -> None:
+        n = req_ids.numel() if n is None else n
+        check(skv_write_back(self.h, _ptr(req_ids), n, _ptr(rows), _stream_handle(stream)), "skv_write_back")
+
+    def assemble(self, req_ids, topk, slots, hits, misses, B: int | None = None, stream=None) -> None:
+        B = req_ids.numel() if B is None else B
+        check(skv_assemble(self.h, _ptr(req_ids), B, _ptr(topk), _ptr(slots), _ptr(hits), _ptr(misses),
+                           _stream_handle(stream)), "skv_assemble")
+
+    def assemble_host(self, req_ids, topk, slots, hits, misses, B: int | None = None, stream=None) -> None:
+        B = len(req_ids) if B is None else B
+        check(skv_assemble_host(self.h, _ptr(req_ids), B, _ptr(topk), _ptr(slots), _ptr(hits), _ptr(misses),
+                                _stream_handle(stream)), "skv_assemble_host")
+
+    # inspection ------------------------------------------------------------
+    def get_device_error(self, stream=None) -> int:
+        bits = ctypes.c_int32()
+        check(skv_get_device_error(self.h, ctypes.byref(bits), _stream_handle(stream)), "skv_get_device_error")
+        return bits.value
+
+    def hot_buffer(self):
+        base, stride = ctypes.c_void_p(), ctypes.c_int64()
+        check(skv_hot_buffer(self.h, ctypes.byref(base), ctypes.byref(stride)), "skv_hot_buffer")
+        return base.value, stride.value
+
+    def pool_rows(self) -> int:
+        base = ctypes.c_void_p()
+        check(skv_pool_rows(self.h, ctypes.byref(base)), "skv_pool_rows")
+        return base.value
+
+    def export_state(self, req: int, tok2slot: bool = True, stream=None):
+        import numpy as np
+        L, S, T = self.cfg.num_layers, self.cfg.hot_slots, self.cfg.max_context
+        s2t = np.empty((L, S), np.int32)
+        ts = np.empty((L, S), np.uint32)
+        lru = np.empty((L, S), np.int32)
+        t2s = np.empty((L, T), np.int32) if tok2slot else None
+        ln = np.zeros(1, np.int64)
+        act = np.zeros(1, np.int32)
+        check(skv_export_state(self.h, req, _ptr(s2t), _ptr(ts), _ptr(t2s), _ptr(lru), _ptr(ln), _ptr(act),
+                               _stream_handle(stream)), "skv_export_state")
+        return {"slot2tok": s2t, "ts": ts, "lru": lru, "tok2slot": t2s, "len": int(ln[0]), "active": int(act[0])}
+
+    def export_hot(self, req: int, stream=None):
+        import numpy as np
+        out = np.empty((self.cfg.num_layers, self.cfg.hot_slots, self.cfg.row_bytes), np.uint8)
+        check(skv_export_hot(self.h, req, _ptr(out), _stream_handle(stream)), "skv_export_hot")
+        return out
+
+    def clock(self, stream=None) -> int:
+        c = ctypes.c_uint32()
+        check(skv_get_clock(self.h, ctypes.byref(c), _stream_handle(stream)), "skv_get_clock")
+        return c.value
+
+    def stats(self, stream=None):
+        a, b, c = ctypes.c_uint64(), ctypes.c_uint64(), ctypes.c_uint64()
+        check(skv_get_stats(self.h, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c), _stream_handle(stream)),
+              "skv_get_stats")
+        return {"calls": a.value, "hits": b.value, "misses": c.value}
+
+    def set_gather_events(self, before=None, after=None) -> None:
+        check(skv_set_gather_events(self.h, before.cuda_event if before is not None else None,
+                                    after.cuda_event if after is not None else None), "skv_set_gather_events")
