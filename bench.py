@@ -164,6 +164,19 @@ def measure_link_gbs(torch, dev):
     return out
 
 
+def event_ms(a, b) -> float:
+    """Elapsed ms between two events that the library recorded (torch does
+    not know they were recorded, so ask the driver directly)."""
+    import ctypes
+    drv = ctypes.CDLL("libcuda.so.1")
+    f = getattr(drv, "cuEventElapsedTime_v2", None) or drv.cuEventElapsedTime
+    ms = ctypes.c_float()
+    rc = f(ctypes.byref(ms), ctypes.c_void_p(a.cuda_event), ctypes.c_void_p(b.cuda_event))
+    if rc != 0:
+        raise RuntimeError(f"cuEventElapsedTime failed: {rc}")
+    return ms.value
+
+
 def hbm_peak_gbs():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -281,6 +294,10 @@ def run_ours(args):
     stream = torch.cuda.Stream(device=dev)
     ev_b = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n_dev)]
     ev_a = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n_dev)]
+    for ev in ev_b + ev_a:  # torch creates the CUDA event lazily, at its first record
+        ev.record(stream)
+    torch.cuda.synchronize()
+    assert all(ev.cuda_event for ev in ev_b + ev_a)
 
     def enqueue(s):
         ctx.set_gather_events(ev_b[s], ev_a[s])
@@ -327,7 +344,7 @@ def run_ours(args):
     H = st1["hits"] - st0["hits"]
     assert st1["calls"] - st0["calls"] == K
     assert ctx.get_device_error() == 0
-    gather_s = sum(ev_b[s].elapsed_time(ev_a[s]) for s in range(W, n_dev)) / 1e3
+    gather_s = sum(event_ms(ev_b[s], ev_a[s]) for s in range(W, n_dev)) / 1e3
     per_step_m = misses[W:].sum(dim=(1, 2)).cpu().numpy().astype(np.int64)
     per_step_h = hits[W:].sum(dim=(1, 2)).cpu().numpy().astype(np.int64)
     assert int(per_step_m.sum()) == M

@@ -122,6 +122,18 @@ void host_copy(uint8_t* dst, const uint8_t* src, size_t n)
     for (auto& t : th) t.join();
 }
 
+// A timing event: during stream capture it must become an external event
+// record node of the graph (a plain record would only be a dependency marker);
+// outside capture it is an ordinary record.
+cudaError_t record_event(cudaEvent_t ev, cudaStream_t stream)
+{
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(stream, &cs);
+    if (e != cudaSuccess) return e;
+    if (cs == cudaStreamCaptureStatusActive) return cudaEventRecordWithFlags(ev, stream, cudaEventRecordExternal);
+    return cudaEventRecord(ev, stream);
+}
+
 }  // namespace
 
 extern "C" {
@@ -295,9 +307,9 @@ skv_status skv_assemble(skv_ctx* ctx, const int32_t* req_ids_dev, int32_t B, con
     const Dev& d = ctx->d;
     SKV_CUDA(skv::launch_validate(d, req_ids_dev, B, topk_dev, stream));
     SKV_CUDA(skv::launch_plan(d, req_ids_dev, B, topk_dev, slots_dev, hits_dev, misses_dev, stream));
-    if (ctx->ev_before) SKV_CUDA(cudaEventRecordWithFlags(ctx->ev_before, stream, cudaEventRecordExternal));
+    if (ctx->ev_before) SKV_CUDA(record_event(ctx->ev_before, stream));
     SKV_CUDA(skv::launch_gather(d, ctx->gather_grid, stream));
-    if (ctx->ev_after) SKV_CUDA(cudaEventRecordWithFlags(ctx->ev_after, stream, cudaEventRecordExternal));
+    if (ctx->ev_after) SKV_CUDA(record_event(ctx->ev_after, stream));
     return SKV_OK;
 }
 

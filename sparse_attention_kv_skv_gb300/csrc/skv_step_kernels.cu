@@ -413,11 +413,15 @@ size_t validate_smem_bytes(int k) { return ((size_t)1 << table_log2_for(k)) * 4;
 
 cudaError_t prepare_step_kernels(int k, int S, int* gather_grid)
 {
+    // the attributes are per function, not per context: allow the largest
+    // (k, S) any context may use, so contexts of different shapes coexist
+    (void)k;
+    (void)S;
     cudaError_t e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)plan_smem_bytes(k, S));
+                                         (int)plan_smem_bytes(kMaxTopk, kMaxSlots));
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(validate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)validate_smem_bytes(k));
+                             (int)validate_smem_bytes(kMaxTopk));
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0, per_sm = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
