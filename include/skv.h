@@ -176,6 +176,27 @@ SKV_API skv_status skv_assemble(skv_ctx *ctx, const int32_t *req_ids_dev, int32_
 SKV_API skv_status skv_assemble_host(skv_ctx *ctx, const int32_t *req_ids, int32_t B, const int32_t *topk, int32_t *slots,
                              int32_t *hits, int32_t *misses, skv_stream_t stream);
 
+/* skv_assemble for callers that cannot allocate device memory when they
+ * call: engines that reserve almost all HBM for their own pools at start-up
+ * and allow no later cudaMalloc, or code that runs inside another
+ * component's stream capture.  It allocates nothing and takes nothing from
+ * the context's scratch: the gather work list lives in a file-scope static
+ * device array of 2^20 (pool row, hot row) entries (8 MiB), which every
+ * device that loads the library holds until the process exits.  Same
+ * arguments, semantics and results as skv_assemble, except:
+ *   - B * L * k must be <= 2^20, else SKV_ERR_INVALID_ARG (with the reason in
+ *     skv_last_cuda_error) and nothing is enqueued;
+ *   - the first call on a device looks up the array's device address (with
+ *     that device current) and caches it: make that first call before any
+ *     stream capture;
+ *   - every call on a device shares the one array: calls that overlap on the
+ *     GPU (other streams, other contexts) race.  Nothing in the array needs
+ *     to start at zero; the step resets its own counter.
+ * The pages describe no counterpart of this entry point. */
+SKV_API skv_status skv_assemble_noalloc(skv_ctx *ctx, const int32_t *req_ids_dev, int32_t B, const int32_t *topk_dev,
+                                        int32_t *slots_dev, int32_t *hits_dev, int32_t *misses_dev,
+                                        skv_stream_t stream);
+
 /* Release a request (lifecycle step "release"): its slot becomes free, its
  * maps are reset and its hot rows zeroed (enqueued on `stream`).  A later
  * skv_publish may hand the same id out again.  SKV_ERR_BAD_REQUEST if req is

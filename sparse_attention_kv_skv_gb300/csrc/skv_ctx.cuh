@@ -1,0 +1,27 @@
+// The context object behind the opaque skv_ctx handle (internal; not ABI).
+#pragma once
+
+#include <vector>
+
+#include "skv.h"
+#include "skv_internal.cuh"
+
+struct skv_ctx {
+    skv_config cfg{};
+    skv::Dev d{};
+    uint8_t* pool_host = nullptr;  // same memory as d.pool (mapped)
+    std::vector<uint8_t> active_h;  // host mirror of the request table
+    int32_t* st_req = nullptr;      // staging for skv_assemble_host
+    int32_t* st_topk = nullptr;
+    int32_t* st_slots = nullptr;
+    int32_t* st_hits = nullptr;
+    int32_t* st_misses = nullptr;
+    uint32_t* host_word = nullptr;  // pinned word for reading the error bits
+    cudaEvent_t ev_before = nullptr, ev_after = nullptr;
+    int gather_grid = 0;
+};
+
+namespace skv {
+// Sets the message returned by skv_last_cuda_error on this thread.
+void set_last_error_message(const char* msg);
+}  // namespace skv

@@ -15,25 +15,9 @@
 #include <thread>
 #include <vector>
 
-#include "skv.h"
-#include "skv_internal.cuh"
+#include "skv_ctx.cuh"
 
 using skv::Dev;
-
-struct skv_ctx {
-    skv_config cfg{};
-    Dev d{};
-    uint8_t* pool_host = nullptr;  // same memory as d.pool (mapped)
-    std::vector<uint8_t> active_h;  // host mirror of the request table
-    int32_t* st_req = nullptr;      // staging for skv_assemble_host
-    int32_t* st_topk = nullptr;
-    int32_t* st_slots = nullptr;
-    int32_t* st_hits = nullptr;
-    int32_t* st_misses = nullptr;
-    uint32_t* host_word = nullptr;  // pinned word for reading the error bits
-    cudaEvent_t ev_before = nullptr, ev_after = nullptr;
-    int gather_grid = 0;
-};
 
 namespace {
 
@@ -135,6 +119,8 @@ cudaError_t record_event(cudaEvent_t ev, cudaStream_t stream)
 }
 
 }  // namespace
+
+void skv::set_last_error_message(const char* msg) { g_last_cuda_error = msg; }
 
 extern "C" {
 

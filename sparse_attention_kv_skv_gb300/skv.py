@@ -59,6 +59,7 @@ def _load():
         "skv_write_back": [vp, vp, i32, vp, vp],
         "skv_assemble": [vp, vp, i32, vp, vp, vp, vp, vp],
         "skv_assemble_host": [vp, vp, i32, vp, vp, vp, vp, vp],
+        "skv_assemble_noalloc": [vp, vp, i32, vp, vp, vp, vp, vp],
         "skv_release": [vp, i32, vp],
         "skv_get_device_error": [vp, P(i32), vp],
         "skv_hot_buffer": [vp, P(vp), P(i64)],
@@ -89,6 +90,7 @@ skv_publish = lib.skv_publish
 skv_write_back = lib.skv_write_back
 skv_assemble = lib.skv_assemble
 skv_assemble_host = lib.skv_assemble_host
+skv_assemble_noalloc = lib.skv_assemble_noalloc
 skv_release = lib.skv_release
 skv_get_device_error = lib.skv_get_device_error
 skv_hot_buffer = lib.skv_hot_buffer
@@ -197,6 +199,13 @@ class Context:
         B = req_ids.numel() if B is None else B
         check(skv_assemble(self.h, _ptr(req_ids), B, _ptr(topk), _ptr(slots), _ptr(hits), _ptr(misses),
                            _stream_handle(stream)), "skv_assemble")
+
+    def assemble_noalloc(self, req_ids, topk, slots, hits, misses, B: int | None = None, stream=None) -> None:
+        """skv_assemble with the gather work list in the library's static
+        device array (allocates nothing; see include/skv.h)."""
+        B = req_ids.numel() if B is None else B
+        check(skv_assemble_noalloc(self.h, _ptr(req_ids), B, _ptr(topk), _ptr(slots), _ptr(hits), _ptr(misses),
+                                   _stream_handle(stream)), "skv_assemble_noalloc")
 
     def assemble_host(self, req_ids, topk, slots, hits, misses, B: int | None = None, stream=None) -> None:
         B = len(req_ids) if B is None else B
