@@ -409,16 +409,17 @@ def run_ours(args):
             "miss_rate": M / max(tokens, 1.0),
             "missed_rows_per_step": M / K,
             "step_roofline_frac": t_roof / elapsed,
-            "roofline": {"bound": "host_link", "kernel": "gather_kernel", "achieved": achieved,
+            "roofline": {"bound": "host_link", "kernel": "plan_kernel<fused> (sparse diff + LRU + gather)",
+                         "achieved": achieved,
                          "peak": link["h2d"], "unit": "GB/s", "frac": achieved / link["h2d"], "traffic": None,
                          "peak_source": "pinned cudaMemcpyAsync host->device, 1 GiB, best of 10, this run",
-                         "gather_share_of_step": gather_s / elapsed,
+                         "kernel_share_of_step": gather_s / elapsed,
                          "hbm": {"peak": hbm_peak, "peak_source": hbm_src,
                                  "algorithmic_bytes_per_step": sum(hbm_algorithmic_bytes(w, int(a), int(b))
                                                                    for a, b in zip(per_step_m, per_step_h)) / K}},
             "link_gbs": link,
             "e2e": e2e,
-            "gpu_launches": K * (3 + (2 if w.appends else 0)),
+            "gpu_launches": K * (2 + (2 if w.appends else 0)),
             "clocks": clocks,
             "cpu_baseline": cpu,
             "setup": {"pool_gb": w.pool_bytes() / 1e9, "pool_fill_s": fill_s},

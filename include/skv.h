@@ -107,7 +107,7 @@ typedef struct {
     int32_t max_requests;  /* R >= 1: request slots */
     int32_t num_layers;    /* L >= 1 */
     int64_t max_context;   /* T_max >= 1: pool rows per (request, layer) */
-    int32_t row_bytes;     /* bytes per KV row; multiple of 16 (1152 for 576 bf16) */
+    int32_t row_bytes;     /* bytes per KV row; multiple of 16, <= 65536 (1152 for 576 bf16) */
     int32_t topk;          /* k, 1 <= k <= 4096 */
     int32_t hot_slots;     /* S, k <= S <= 16384 */
     int32_t max_batch;     /* largest B of skv_assemble / n of skv_write_back */
@@ -159,7 +159,9 @@ SKV_API skv_status skv_write_back(skv_ctx *ctx, const int32_t *req_ids_dev, int3
  *   3. LRU allocation: the misses take the least recently used non-hit slots
  *      (rule above); evicted tokens leave tok2slot;
  *   4. gather: copy each missed token's row from the host pool into its slot
- *      (16-byte loads through the mapped pool over the host link);
+ *      (16-byte loads through the mapped pool over the host link; steps 2-4
+ *      and 5 run in one kernel, one CTA per (b, l), so planning overlaps the
+ *      host-link traffic of other units);
  *   5. emit the fixed-shape slot tensor and the per-(b,l) hit and miss counts
  *      (hits_dev / misses_dev [B][L] int32).
  * The hot row of (request r, layer l, slot s) is at
@@ -237,7 +239,8 @@ SKV_API skv_status skv_get_clock(skv_ctx *ctx, uint32_t *clock, skv_stream_t str
 SKV_API skv_status skv_get_stats(skv_ctx *ctx, uint64_t *calls, uint64_t *hits, uint64_t *misses, skv_stream_t stream);
 
 /* Optional timing hooks: when set (non-null), skv_assemble records `before`
- * just before its gather kernel and `after` just after it on the call's
+ * just before the kernel that performs the gather (the fused plan + gather
+ * kernel; only validation runs before it) and `after` just after it on the call's
  * stream (external event records, so they also work inside a captured
  * graph).  Pass two nulls to clear; passing exactly one null is
  * SKV_ERR_INVALID_ARG.  The events belong to the caller. */

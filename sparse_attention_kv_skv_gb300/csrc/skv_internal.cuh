@@ -10,7 +10,7 @@ namespace skv {
 constexpr int kMaxTopk = 4096;    // k limit (plan kernel keeps <= 8 entries per thread)
 constexpr int kMaxSlots = 16384;  // S limit (uint16 LRU entries, shared-memory budget)
 constexpr int kPlanThreads = 512;
-constexpr int kValidateThreads = 256;
+constexpr int kValidateThreads = 512;
 constexpr int kGatherThreads = 256;
 constexpr int kLifecycleThreads = 256;
 
@@ -19,8 +19,9 @@ enum : int {
     CTL_CLOCK = 0,     // step clock: successful assemble calls
     CTL_ERR = 1,       // sticky error bits (SKV_DEVERR_*)
     CTL_ERR_CALL = 2,  // error bits found by the running assemble call, committed by the gather kernel
-    CTL_JOBS = 3,      // rows queued for the gather by the running assemble call
-    CTL_WORDS = 4
+    CTL_JOBS = 3,      // rows queued for the gather by the running assemble call (job-list path)
+    CTL_DONE = 4,      // CTAs of the fused plan+gather kernel that have finished (last one commits)
+    CTL_WORDS = 5
 };
 enum : int { STAT_CALLS = 0, STAT_HITS = 1, STAT_MISSES = 2, STAT_WORDS = 3 };
 
@@ -53,6 +54,10 @@ cudaError_t launch_validate(const Dev& d, const int32_t* req_ids, int B, const i
 cudaError_t launch_plan(const Dev& d, const int32_t* req_ids, int B, const int32_t* topk, int32_t* slots,
                         int32_t* hits, int32_t* misses, cudaStream_t st);
 cudaError_t launch_gather(const Dev& d, int grid, cudaStream_t st);
+// plan + gather fused: each (b, l) CTA copies its own misses right after
+// planning them; the last CTA to finish commits the call.
+cudaError_t launch_plan_gather(const Dev& d, const int32_t* req_ids, int B, const int32_t* topk, int32_t* slots,
+                               int32_t* hits, int32_t* misses, cudaStream_t st);
 cudaError_t prepare_step_kernels(int k, int S, int* gather_grid);
 
 // Lifecycle kernels.

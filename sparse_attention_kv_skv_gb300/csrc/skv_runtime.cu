@@ -146,6 +146,7 @@ skv_status skv_create(const skv_config* cfg, skv_ctx** out)
     *out = nullptr;
     const skv_config c = *cfg;
     if (c.max_requests < 1 || c.num_layers < 1 || c.max_context < 1 || c.row_bytes < 16 || c.row_bytes % 16 != 0 ||
+        c.row_bytes > 65536 ||
         c.topk < 1 || c.topk > skv::kMaxTopk || c.hot_slots < c.topk || c.hot_slots > skv::kMaxSlots ||
         c.max_batch < 1 || c.device < 0)
         return SKV_ERR_INVALID_ARG;
@@ -292,9 +293,8 @@ skv_status skv_assemble(skv_ctx* ctx, const int32_t* req_ids_dev, int32_t B, con
     DeviceGuard g(ctx->cfg.device);
     const Dev& d = ctx->d;
     SKV_CUDA(skv::launch_validate(d, req_ids_dev, B, topk_dev, stream));
-    SKV_CUDA(skv::launch_plan(d, req_ids_dev, B, topk_dev, slots_dev, hits_dev, misses_dev, stream));
     if (ctx->ev_before) SKV_CUDA(record_event(ctx->ev_before, stream));
-    SKV_CUDA(skv::launch_gather(d, ctx->gather_grid, stream));
+    SKV_CUDA(skv::launch_plan_gather(d, req_ids_dev, B, topk_dev, slots_dev, hits_dev, misses_dev, stream));
     if (ctx->ev_after) SKV_CUDA(record_event(ctx->ev_after, stream));
     return SKV_OK;
 }

@@ -52,19 +52,54 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* total,
     return before + x - v;
 }
 
+// block-wide exclusive max over int32 values (identity -1); same calling
+// rules as block_excl_scan.
+__device__ __forceinline__ int32_t block_excl_max(int32_t v, int32_t* sh)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int32_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+        if (lane >= o) x = max(x, y);
+    }
+    int32_t before_in_warp = __shfl_up_sync(0xFFFFFFFFu, x, 1);
+    if (lane == 0) before_in_warp = -1;
+    if (lane == 31) sh[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int32_t w = lane < nw ? sh[lane] : -1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int32_t y = __shfl_up_sync(0xFFFFFFFFu, w, o);
+            if (lane >= o) w = max(w, y);
+        }
+        if (lane < nw) sh[lane] = w;
+    }
+    __syncthreads();
+    const int32_t before = warp > 0 ? sh[warp - 1] : -1;
+    __syncthreads();
+    return max(before, before_in_warp);
+}
+
 __device__ __forceinline__ bool bit_test(const uint32_t* bm, int s) { return (bm[s >> 5] >> (s & 31)) & 1u; }
 
 // ---------------------------------------------------------------------------
 // validate: one CTA per (b, l).  Checks the request id (in range, active, not
 // repeated in the batch -- the l == 0 CTA of each b compares with the earlier
-// entries) and every Top-k entry (-1 or in [0, len)), and finds repeated
-// tokens with an open-addressing set in shared memory.  Error bits go to
-// CTL_ERR_CALL; nothing else is written except the reset of the gather list.
+// entries) and every Top-k entry (-1 or in [0, len)).  Repeated tokens: a row
+// whose non-padding entries are strictly ascending has none (the common case:
+// Top-k rows usually come sorted); any other row goes through an
+// open-addressing set in shared memory.  Error bits go to CTL_ERR_CALL;
+// nothing else is written except the reset of the job-list counter.
 // ---------------------------------------------------------------------------
+constexpr int kValIpt = kMaxTopk / kValidateThreads;
+
 __global__ void __launch_bounds__(kValidateThreads) validate_kernel(Dev d, const int32_t* __restrict__ req_ids, int B,
                                                                     const int32_t* __restrict__ topk, int table_log2)
 {
     extern __shared__ uint32_t table[];
+    __shared__ int32_t scan_sh[32];
     __shared__ uint32_t flags;
     if (blockIdx.x == 0 && threadIdx.x == 0) d.ctl[CTL_JOBS] = 0;
     if (d.ctl[CTL_ERR] != 0) return;  // sticky error: the call is a no-op
@@ -78,29 +113,53 @@ __global__ void __launch_bounds__(kValidateThreads) validate_kernel(Dev d, const
     if (l == 0)
         for (int j = threadIdx.x; j < b; j += blockDim.x)
             if (req_ids[j] == r) f |= DEVERR_BAD_REQUEST;
-    const int H = 1 << table_log2;
-    for (int j = threadIdx.x; j < H; j += blockDim.x) table[j] = kEmpty;
     if (threadIdx.x == 0) flags = 0;
-    __syncthreads();
     const int64_t len = d.len[r];
-    const int32_t* row = topk + (size_t)blockIdx.x * d.k;
-    for (int i = threadIdx.x; i < d.k; i += blockDim.x) {
-        const int32_t t = row[i];
-        if (t == -1) continue;
-        if (t < 0 || (int64_t)t >= len) {
-            f |= DEVERR_BAD_INDEX;
-            continue;
+    const int k = d.k;
+    const int32_t* row = topk + (size_t)blockIdx.x * k;
+    // blocked arrangement: thread t holds entries [t*ipt, t*ipt + ipt)
+    const int ipt = (k + blockDim.x - 1) / blockDim.x;
+    const int i0 = threadIdx.x * ipt;
+    int32_t tok[kValIpt];
+    int32_t first = -1, prev = -1;
+    bool asc = true;
+#pragma unroll
+    for (int j = 0; j < kValIpt; ++j) {
+        tok[j] = -1;
+        if (j < ipt && i0 + j < k) {
+            const int32_t t = row[i0 + j];
+            tok[j] = t;
+            if (t == -1) continue;
+            if (t < 0 || (int64_t)t >= len) f |= DEVERR_BAD_INDEX;
+            if (prev != -1 && t <= prev) asc = false;
+            if (t < 0) asc = false;
+            if (first == -1) first = t;
+            prev = t;
         }
-        uint32_t h = ((uint32_t)t * 2654435761u) >> (32 - table_log2);
-        // H >= 2k, so an empty cell is always reachable: at most H probes
-        for (int probe = 0; probe < H; ++probe) {
-            const uint32_t prev = atomicCAS(&table[h], kEmpty, (uint32_t)t);
-            if (prev == kEmpty) break;
-            if (prev == (uint32_t)t) {
-                f |= DEVERR_DUPLICATE;
-                break;
+    }
+    // the row is strictly ascending iff every segment is and each segment's
+    // first entry exceeds the largest entry before it
+    const int32_t before = block_excl_max(prev, scan_sh);
+    if (first != -1 && first <= before) asc = false;
+    if (!__syncthreads_and(asc)) {
+        const int H = 1 << table_log2;
+        for (int j = threadIdx.x; j < H; j += blockDim.x) table[j] = kEmpty;
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < kValIpt; ++j) {
+            const int32_t t = tok[j];
+            if (j >= ipt || t < 0 || (int64_t)t >= len) continue;  // padding, out of range (already flagged)
+            uint32_t h = ((uint32_t)t * 2654435761u) >> (32 - table_log2);
+            // H >= 2k, so an empty cell is always reachable: at most H probes
+            for (int probe = 0; probe < H; ++probe) {
+                const uint32_t p = atomicCAS(&table[h], kEmpty, (uint32_t)t);
+                if (p == kEmpty) break;
+                if (p == (uint32_t)t) {
+                    f |= DEVERR_DUPLICATE;
+                    break;
+                }
+                h = (h + 1) & (uint32_t)(H - 1);
             }
-            h = (h + 1) & (uint32_t)(H - 1);
         }
     }
     if (f) atomicOr(&flags, f);
@@ -156,6 +215,52 @@ __device__ inline PlanSmem carve_plan_smem(uint8_t* base, int k, int S)
     return m;
 }
 
+__device__ __forceinline__ int4 ld_stream(const int4* p)
+{
+    int4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.s32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+__device__ __forceinline__ void st_stream(int4* p, int4 v)
+{
+    asm volatile("st.global.cs.v4.s32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// Commit of a call by the last CTA of the fused kernel to finish: every CTA
+// has read the clock by then, so it can advance.  All threads of the CTA call
+// this.  No CTA waits for another.
+__device__ __forceinline__ void finish_call(const Dev& d)
+{
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const uint32_t done = atomicAdd(&d.ctl[CTL_DONE], 1u);
+        if (done == gridDim.x - 1) {
+            __threadfence();
+            const uint32_t e = atomicAdd(&d.ctl[CTL_ERR_CALL], 0u);
+            if (atomicAdd(&d.ctl[CTL_ERR], 0u) == 0 && e == 0) {
+                d.ctl[CTL_CLOCK] += 1u;
+                d.stats[STAT_CALLS] += 1ull;
+            }
+            d.ctl[CTL_ERR] |= e;
+            d.ctl[CTL_ERR_CALL] = 0u;
+            d.ctl[CTL_DONE] = 0u;
+        }
+    }
+}
+
+constexpr int kFusedUnroll = 4;
+
+// kFused = false: the misses become jobs of the global work list, copied by
+// gather_kernel.  kFused = true: the CTA copies its own misses (pool row ->
+// hot row, 16-byte chunks) right after planning them, so the planning of
+// later units overlaps the host-link traffic of earlier ones; each CTA walks
+// its own pool region in ascending token order, which keeps the GPU's
+// translation of the mapped pool local.
+template <bool kFused, int CPR_CONST>
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Dev d, const int32_t* __restrict__ req_ids,
                                                             const int32_t* __restrict__ topk,
                                                             int32_t* __restrict__ slots_out,
@@ -176,6 +281,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Dev d, const int32_t
             hits_out[blockIdx.x] = -1;
             misses_out[blockIdx.x] = -1;
         }
+        if (kFused) finish_call(d);
         return;
     }
 
@@ -299,10 +405,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Dev d, const int32_t
         if (s < S && (bit_test(sm.hitbits, s) || bit_test(sm.vicbits, s))) sm.lru_new[untouched + pos++] = (uint16_t)s;
     }
 
-    // E. map update, slot emission, gather jobs
-    if (tid == 0) job_base_sh = m ? atomicAdd(&d.ctl[CTL_JOBS], (uint32_t)m) : 0u;
-    __syncthreads();
-    const uint32_t job_base = job_base_sh;
+    // E. map update and slot emission (plus gather jobs on the job-list path)
+    if (!kFused) {
+        if (tid == 0) job_base_sh = m ? atomicAdd(&d.ctl[CTL_JOBS], (uint32_t)m) : 0u;
+        __syncthreads();
+    }
     for (int j = tid; j < m; j += NT) {
         const int v = sm.victim[j];
         const unsigned long long key = sm.miss[j];
@@ -314,7 +421,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Dev d, const int32_t
         t2s[t] = v;
         tsu[v] = now1;
         sm.out[i] = v;
-        d.jobs[job_base + j] = make_uint2((uint32_t)(u * d.T_max + t), (uint32_t)(u * S + v));
+        if (!kFused) d.jobs[job_base_sh + j] = make_uint2((uint32_t)(u * d.T_max + t), (uint32_t)(u * S + v));
     }
     __syncthreads();
 
@@ -324,6 +431,34 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Dev d, const int32_t
         hits_out[blockIdx.x] = h;
         misses_out[blockIdx.x] = m;
         if (h) atomicAdd(&d.stats[STAT_HITS], (unsigned long long)h);
+        if (kFused && m) atomicAdd(&d.stats[STAT_MISSES], (unsigned long long)m);
+    }
+
+    if (kFused) {
+        // F. gather: pool row (u, token) -> hot row (u, victim slot)
+        const int cpr = CPR_CONST > 0 ? CPR_CONST : d.row_bytes / 16;
+        const int4* __restrict__ src = reinterpret_cast<const int4*>(d.pool) + (size_t)u * d.T_max * cpr;
+        int4* __restrict__ dst = reinterpret_cast<int4*>(d.hot) + (size_t)u * S * cpr;
+        const int chunks = m * cpr;
+        for (int base = tid; base < chunks; base += NT * kFusedUnroll) {
+            int4 v[kFusedUnroll];
+            size_t o[kFusedUnroll];
+#pragma unroll
+            for (int j = 0; j < kFusedUnroll; ++j) {
+                const int c = base + j * NT;
+                if (c < chunks) {
+                    const int jj = c / cpr;
+                    const int w = c - jj * cpr;
+                    const int32_t t = (int32_t)(sm.miss[jj] >> 32);
+                    o[j] = (size_t)sm.victim[jj] * cpr + w;
+                    v[j] = ld_stream(src + (size_t)t * cpr + w);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kFusedUnroll; ++j)
+                if (base + j * NT < chunks) st_stream(dst + o[j], v[j]);
+        }
+        finish_call(d);
     }
 }
 
@@ -335,20 +470,6 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Dev d, const int32_t
 // the call: clock + 1 and statistics on success, error bits into the sticky
 // word.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ int4 ld_stream(const int4* p)
-{
-    int4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.s32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-__device__ __forceinline__ void st_stream(int4* p, int4 v)
-{
-    asm volatile("st.global.cs.v4.s32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                 : "memory");
-}
-
 template <int CPR_CONST, int U>
 __global__ void __launch_bounds__(kGatherThreads) gather_kernel(Dev d, int cpr_rt)
 {
@@ -417,8 +538,12 @@ cudaError_t prepare_step_kernels(int k, int S, int* gather_grid)
     // (k, S) any context may use, so contexts of different shapes coexist
     (void)k;
     (void)S;
-    cudaError_t e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)plan_smem_bytes(kMaxTopk, kMaxSlots));
+    const int plan_max = (int)plan_smem_bytes(kMaxTopk, kMaxSlots);
+    cudaError_t e = cudaFuncSetAttribute(plan_kernel<false, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, plan_max);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(plan_kernel<true, 72>, cudaFuncAttributeMaxDynamicSharedMemorySize, plan_max);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(plan_kernel<true, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, plan_max);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(validate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)validate_smem_bytes(kMaxTopk));
@@ -443,7 +568,19 @@ cudaError_t launch_validate(const Dev& d, const int32_t* req_ids, int B, const i
 cudaError_t launch_plan(const Dev& d, const int32_t* req_ids, int B, const int32_t* topk, int32_t* slots,
                         int32_t* hits, int32_t* misses, cudaStream_t st)
 {
-    plan_kernel<<<B * d.L, kPlanThreads, plan_smem_bytes(d.k, d.S), st>>>(d, req_ids, topk, slots, hits, misses);
+    plan_kernel<false, 0>
+        <<<B * d.L, kPlanThreads, plan_smem_bytes(d.k, d.S), st>>>(d, req_ids, topk, slots, hits, misses);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_plan_gather(const Dev& d, const int32_t* req_ids, int B, const int32_t* topk, int32_t* slots,
+                               int32_t* hits, int32_t* misses, cudaStream_t st)
+{
+    const size_t smem = plan_smem_bytes(d.k, d.S);
+    if (d.row_bytes == 1152)
+        plan_kernel<true, 72><<<B * d.L, kPlanThreads, smem, st>>>(d, req_ids, topk, slots, hits, misses);
+    else
+        plan_kernel<true, 0><<<B * d.L, kPlanThreads, smem, st>>>(d, req_ids, topk, slots, hits, misses);
     return cudaGetLastError();
 }
 

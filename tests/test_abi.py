@@ -65,6 +65,7 @@ def test_host_argument_checks_need_no_gpu(lib_path):
         skv.skv_config(1, 1, 10, 1152, 4, 20000, 1, 0),   # S above the limit
         skv.skv_config(1 << 16, 64, 1 << 20, 1152, 4, 8, 1, 0),  # R*L*T_max >= 2^32
         skv.skv_config(1, 1, 10, 1152, 4, 8, 0, 0),       # max_batch 0
+        skv.skv_config(1, 1, 10, 65552, 4, 8, 1, 0),      # rows above 64 KiB
     ]
     for c in bad:
         assert skv.skv_create(ctypes.byref(c), ctypes.byref(h)) == skv.SKV_ERR_INVALID_ARG
