@@ -187,6 +187,24 @@ def hbm_peak_gbs():
     return 6800.0, "fallback 6.8 TB/s"
 
 
+# DRAM traffic of the fused kernel from the ncu capture summarised in
+# profiles/plan_gather_kernel_c2_16k_b64.md (one steady c2 step, 512 units):
+# dram__bytes_read.sum + dram__bytes_write.sum.  Valid only while the kernel
+# source is the one that was captured; scaled to other workloads by units.
+PROFILED_TRAFFIC = {"source": "sparse_attention_kv_skv_gb300/csrc/skv_step_kernels.cu",
+                    "sha256": "f3ae9416066b64aaef853af5f4170d6cb3ebf50f72a3e8b0a6143717e2713529",
+                    "units": 512, "dram_bytes": 42.706432e6 + 194.308096e6,
+                    "summary": "profiles/plan_gather_kernel_c2_16k_b64.md"}
+
+
+def profiled_traffic(w: wl.Workload):
+    import hashlib
+    src = os.path.join(ROOT, PROFILED_TRAFFIC["source"])
+    if hashlib.sha256(open(src, "rb").read()).hexdigest() != PROFILED_TRAFFIC["sha256"]:
+        return None  # the kernel changed since the counters were taken
+    return PROFILED_TRAFFIC["dram_bytes"] * (w.B * w.L) / PROFILED_TRAFFIC["units"]
+
+
 def hbm_algorithmic_bytes(w: wl.Workload, M: int, hits: int) -> int:
     """Bytes one step must move in HBM (besides the link reads): Top-k read,
     tok2slot probes, slot tensor write, LRU order read+write, clock stamps of
@@ -317,9 +335,15 @@ def run_ours(args):
                 graphs.append(g)
         ctx.set_gather_events(None, None)
     torch.cuda.synchronize()
+    warm = []  # (ms, missed rows) of each warm-up step; step 0 is cold (every entry misses)
     with torch.cuda.stream(stream):
         for s in range(W):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
             enqueue(s)
+            b.record(stream)
+            b.synchronize()
+            warm.append((a.elapsed_time(b), int(misses[s].sum())))
     torch.cuda.synchronize()
     st0 = ctx.stats()
     if dist is not None:
@@ -411,12 +435,19 @@ def run_ours(args):
             "step_roofline_frac": t_roof / elapsed,
             "roofline": {"bound": "host_link", "kernel": "plan_kernel<fused> (sparse diff + LRU + gather)",
                          "achieved": achieved,
-                         "peak": link["h2d"], "unit": "GB/s", "frac": achieved / link["h2d"], "traffic": None,
+                         "peak": link["h2d"], "unit": "GB/s", "frac": achieved / link["h2d"],
+                         "traffic": profiled_traffic(w),
+                         "traffic_source": "dram read+write of one c2 step captured with ncu, scaled by units "
+                                           f"({PROFILED_TRAFFIC['summary']}); host-link reads = 1152 B per missed row",
+                         "link_bytes_per_step": M * rb / K,
                          "peak_source": "pinned cudaMemcpyAsync host->device, 1 GiB, best of 10, this run",
                          "kernel_share_of_step": gather_s / elapsed,
                          "hbm": {"peak": hbm_peak, "peak_source": hbm_src,
                                  "algorithmic_bytes_per_step": sum(hbm_algorithmic_bytes(w, int(a), int(b))
                                                                    for a, b in zip(per_step_m, per_step_h)) / K}},
+            "cold_step": {"ms": warm[0][0], "missed_rows": warm[0][1],
+                          "gbs": warm[0][1] * rb / warm[0][0] / 1e6} if rank == 0 else None,
+            "warmup_steps_ms": [round(t, 3) for t, _ in warm],
             "link_gbs": link,
             "e2e": e2e,
             "gpu_launches": K * (2 + (2 if w.appends else 0)),
