@@ -1,0 +1,56 @@
+"""The benchmark's multi-rank harness on CPU (gloo, world size 2): each rank
+runs its own replica with its own seed; elapsed time is the max over ranks and
+work is summed.  No GPU and no data-path collective are involved."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _rank_main(rank, world, port, out):
+    os.environ.update({"MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port), "RANK": str(rank),
+                       "WORLD_SIZE": str(world), "LOCAL_RANK": str(rank)})
+    import bench
+    import skv_workload as wl
+    ws, r, local = bench.dist_env()
+    dist = bench.init_dist(ws)
+    w = bench.rank_seed(wl.WORKLOADS["c1_tiny"], r)
+    # a replica's input: this rank's first Top-k step
+    topk = wl.TopkStream(w, nthreads=1).step(0, [w.ctx] * w.B)
+    elapsed, moved, tokens = bench.reduce_results(dist, 1.0 + r, 100.0 * (r + 1), 10.0)
+    out.put((r, (ws, r, local), w.seed, int(topk.sum()), elapsed, moved, tokens))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_rank_harness_reduces_and_seeds_independently():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    (r0, env0, seed0, sum0, e0, m0, t0), (r1, env1, seed1, sum1, e1, m1, t1) = res
+    assert env0 == (2, 0, 0) and env1 == (2, 1, 1)
+    assert seed0 != seed1 and sum0 != sum1          # independent replicas
+    assert e0 == e1 == 2.0                           # max over ranks
+    assert m0 == m1 == 300.0 and t0 == t1 == 20.0    # work summed over ranks
+
+
+def test_single_rank_needs_no_process_group():
+    import bench
+    assert bench.init_dist(1) is None
+    assert bench.reduce_results(None, 1.5, 2.0, 3.0) == (1.5, 2.0, 3.0)
