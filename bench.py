@@ -410,6 +410,7 @@ def run_ours(args):
                "assembled_tokens_per_s": tps}
     if rank == 0:
         achieved = M * rb / gather_s / 1e9
+        kname = "plan_kernel<fused> (sparse diff + LRU + gather)"
         out = {
             "metric": METRIC,
             "value": bytes_all / elapsed_max / 1e9,
@@ -433,7 +434,7 @@ def run_ours(args):
             "miss_rate": M / max(tokens, 1.0),
             "missed_rows_per_step": M / K,
             "step_roofline_frac": t_roof / elapsed,
-            "roofline": {"bound": "host_link", "kernel": "plan_kernel<fused> (sparse diff + LRU + gather)",
+            "roofline": {"bound": "host_link", "kernel": kname,
                          "achieved": achieved,
                          "peak": link["h2d"], "unit": "GB/s", "frac": achieved / link["h2d"],
                          "traffic": profiled_traffic(w),

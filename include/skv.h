@@ -239,7 +239,7 @@ SKV_API skv_status skv_get_clock(skv_ctx *ctx, uint32_t *clock, skv_stream_t str
 SKV_API skv_status skv_get_stats(skv_ctx *ctx, uint64_t *calls, uint64_t *hits, uint64_t *misses, skv_stream_t stream);
 
 /* Optional timing hooks: when set (non-null), skv_assemble records `before`
- * just before the kernel that performs the gather (the fused plan + gather
+ * just before the kernel that moves the missing rows (the fused plan + gather
  * kernel; only validation runs before it) and `after` just after it on the call's
  * stream (external event records, so they also work inside a captured
  * graph).  Pass two nulls to clear; passing exactly one null is

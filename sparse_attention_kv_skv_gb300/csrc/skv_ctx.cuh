@@ -19,6 +19,7 @@ struct skv_ctx {
     uint32_t* host_word = nullptr;  // pinned word for reading the error bits
     cudaEvent_t ev_before = nullptr, ev_after = nullptr;
     int gather_grid = 0;
+    int plan_resident = 1;  // fused-kernel CTAs resident at once (L2 prefetch budget)
 };
 
 namespace skv {

@@ -8,6 +8,7 @@
 // back and release ("XM-Sparse: Netpreme X-Mem ...", section on the SGLang
 // HiSparse integration).
 
+#include <cstdio>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -61,6 +62,8 @@ bool is_device_pointer(const void* p)
     return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
 }
 
+void free_pool(skv_ctx* x);
+
 void free_ctx(skv_ctx* c)
 {
     if (!c) return;
@@ -81,8 +84,24 @@ void free_ctx(skv_ctx* c)
     cudaFree(c->st_hits);
     cudaFree(c->st_misses);
     if (c->host_word) cudaFreeHost(c->host_word);
-    if (c->pool_host) cudaFreeHost(c->pool_host);
+    free_pool(c);
     delete c;
+}
+
+// The host pool: pinned and mapped for the device with cudaHostAlloc.  (A
+// huge-page mapping registered with cudaHostRegister was tried: a stand-alone
+// gather over it starts faster, but once the CPU writes the published rows into
+// the registered range, device reads of it run one to two orders of magnitude
+// below link speed for many steps on GB300, so it is not used.)
+cudaError_t alloc_pool(skv_ctx* x, size_t bytes)
+{
+    return cudaHostAlloc((void**)&x->pool_host, bytes, cudaHostAllocMapped | cudaHostAllocPortable);
+}
+
+void free_pool(skv_ctx* x)
+{
+    if (x->pool_host) cudaFreeHost(x->pool_host);
+    x->pool_host = nullptr;
 }
 
 // Parallel host memcpy for large publishes from host memory.
@@ -184,7 +203,7 @@ skv_status skv_create(const skv_config* cfg, skv_ctx** out)
     } while (0)
 
     const size_t pool_bytes = (size_t)units * c.max_context * c.row_bytes;
-    SKV_TRY(cudaHostAlloc((void**)&x->pool_host, pool_bytes, cudaHostAllocMapped | cudaHostAllocPortable));
+    SKV_TRY(alloc_pool(x, pool_bytes));
     SKV_TRY(cudaHostGetDevicePointer((void**)&d.pool, x->pool_host, 0));
     SKV_TRY(cudaHostAlloc((void**)&x->host_word, 64, cudaHostAllocDefault));
     SKV_TRY(cudaMalloc(&d.tok2slot, (size_t)units * c.max_context * 4));
@@ -215,6 +234,7 @@ skv_status skv_create(const skv_config* cfg, skv_ctx** out)
     SKV_TRY(cudaMemset(d.stats, 0, skv::STAT_WORDS * 8));
     SKV_TRY(skv::launch_init_lru_all(d, 0));
     SKV_TRY(skv::prepare_step_kernels(c.topk, c.hot_slots, &x->gather_grid));
+    x->plan_resident = skv::plan_resident_ctas(c.topk, c.hot_slots);
     SKV_TRY(cudaDeviceSynchronize());
 #undef SKV_TRY
     *out = x;
@@ -294,7 +314,8 @@ skv_status skv_assemble(skv_ctx* ctx, const int32_t* req_ids_dev, int32_t B, con
     const Dev& d = ctx->d;
     SKV_CUDA(skv::launch_validate(d, req_ids_dev, B, topk_dev, stream));
     if (ctx->ev_before) SKV_CUDA(record_event(ctx->ev_before, stream));
-    SKV_CUDA(skv::launch_plan_gather(d, req_ids_dev, B, topk_dev, slots_dev, hits_dev, misses_dev, stream));
+    SKV_CUDA(skv::launch_plan_gather(d, req_ids_dev, B, topk_dev, slots_dev, hits_dev, misses_dev, ctx->plan_resident,
+                                     stream));
     if (ctx->ev_after) SKV_CUDA(record_event(ctx->ev_after, stream));
     return SKV_OK;
 }

@@ -84,6 +84,13 @@ __device__ __forceinline__ int32_t block_excl_max(int32_t v, int32_t* sh)
 
 __device__ __forceinline__ bool bit_test(const uint32_t* bm, int s) { return (bm[s >> 5] >> (s & 31)) & 1u; }
 
+// Programmatic dependent launch: the validate kernel lets the plan kernel start
+// early; the plan kernel waits for validate's completion (and memory) before
+// its first global write.  Both are no-ops without the launch attribute.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+
 // ---------------------------------------------------------------------------
 // validate: one CTA per (b, l).  Checks the request id (in range, active, not
 // repeated in the batch -- the l == 0 CTA of each b compares with the earlier
@@ -101,6 +108,7 @@ __global__ void __launch_bounds__(kValidateThreads) validate_kernel(Dev d, const
     extern __shared__ uint32_t table[];
     __shared__ int32_t scan_sh[32];
     __shared__ uint32_t flags;
+    pdl_launch_dependents();  // the plan kernel may start its read-only work now
     if (blockIdx.x == 0 && threadIdx.x == 0) d.ctl[CTL_JOBS] = 0;
     if (d.ctl[CTL_ERR] != 0) return;  // sticky error: the call is a no-op
     const int b = blockIdx.x / d.L, l = blockIdx.x % d.L;
@@ -254,28 +262,190 @@ __device__ __forceinline__ void finish_call(const Dev& d)
 
 constexpr int kFusedUnroll = 4;
 
+// Fetch `bytes` (multiple of 16, 16-byte aligned) at a global address into L2
+// without waiting for it.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // kFused = false: the misses become jobs of the global work list, copied by
 // gather_kernel.  kFused = true: the CTA copies its own misses (pool row ->
 // hot row, 16-byte chunks) right after planning them, so the planning of
 // later units overlaps the host-link traffic of earlier ones; each CTA walks
 // its own pool region in ascending token order, which keeps the GPU's
 // translation of the mapped pool local.
+//
+// Everything up to the new LRU order (phases A-D) only reads global memory
+// and works in shared memory, so it may run before validation has finished:
+// indices are bounds-checked against the allocation (not against len) before
+// any load, and nothing global is written until pdl_wait() has returned and
+// the call is known to be accepted.  `prefetch_rows` caps how many of this
+// unit's missing rows are prefetched into L2 as soon as they are known (a
+// budget so that all resident CTAs' prefetches fit in L2).
 template <bool kFused, int CPR_CONST>
-__global__ void __launch_bounds__(kPlanThreads) plan_kernel(Dev d, const int32_t* __restrict__ req_ids,
+__global__ void __launch_bounds__(kPlanThreads, 3) plan_kernel(Dev d, const int32_t* __restrict__ req_ids,
                                                             const int32_t* __restrict__ topk,
                                                             int32_t* __restrict__ slots_out,
                                                             int32_t* __restrict__ hits_out,
-                                                            int32_t* __restrict__ misses_out)
+                                                            int32_t* __restrict__ misses_out, int prefetch_rows)
 {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     __shared__ uint32_t scan_sh[32];
     __shared__ uint32_t job_base_sh;
     const int tid = threadIdx.x, NT = blockDim.x;
     const int k = d.k, S = d.S;
+    const int cpr = CPR_CONST > 0 ? CPR_CONST : d.row_bytes / 16;
     const int32_t* row = topk + (size_t)blockIdx.x * k;
     int32_t* out = slots_out + (size_t)blockIdx.x * k;
 
-    if ((d.ctl[CTL_ERR] | d.ctl[CTL_ERR_CALL]) != 0) {  // rejected call: -1 outputs, no state change
+    PlanSmem sm = carve_plan_smem(smem_raw, k, S);
+    const int b = blockIdx.x / d.L, l = blockIdx.x % d.L;
+    const int32_t r = req_ids[b];
+    const bool r_ok = r >= 0 && r < d.R;  // uniform over the CTA; validation decides the rest
+    const int64_t u = (int64_t)(r_ok ? r : 0) * d.L + l;
+    int32_t* t2s = d.tok2slot + u * d.T_max;
+    int32_t* s2t = d.slot2tok + u * S;
+    uint32_t* tsu = d.ts + u * S;
+    uint16_t* lru = d.lru + u * S;
+    const int SW = (S + 31) / 32;
+    const int ipt = (k + NT - 1) / NT;
+    const int i0 = tid * ipt;
+    int m = 0, h = 0;
+
+    if (r_ok) {
+        for (int w = tid; w < SW; w += NT) {
+            sm.hitbits[w] = 0u;
+            sm.vicbits[w] = 0u;
+        }
+        if ((S & 7) == 0) {  // LRU order, 8 slots per 16-byte load
+            const uint4* src = reinterpret_cast<const uint4*>(lru);
+            uint4* dst = reinterpret_cast<uint4*>(sm.lru_old);
+            for (int p = tid; p < S / 8; p += NT) dst[p] = src[p];
+        } else {
+            for (int p = tid; p < S; p += NT) sm.lru_old[p] = lru[p];
+        }
+
+        // A. sparse diff: all row loads, then all (independent) probes; in
+        // sm.out a hit holds its slot, a miss -2 (until phase E), padding -1
+        int32_t tok[kMaxIpt];
+        int32_t hit_slot[kMaxIpt];
+#pragma unroll
+        for (int j = 0; j < kMaxIpt; ++j) tok[j] = (j < ipt && i0 + j < k) ? row[i0 + j] : -1;
+#pragma unroll
+        for (int j = 0; j < kMaxIpt; ++j) {
+            const int32_t t = tok[j];
+            hit_slot[j] = (t >= 0 && (int64_t)t < d.T_max) ? t2s[t] : -1;
+        }
+        __syncthreads();  // bitmaps zeroed, LRU order loaded
+        uint32_t missmask = 0, nmiss = 0, nhit = 0;
+#pragma unroll
+        for (int j = 0; j < kMaxIpt; ++j) {
+            const int i = i0 + j;
+            if (j >= ipt || i >= k) continue;
+            const int32_t t = tok[j], s = hit_slot[j];
+            if (t < 0 || (int64_t)t >= d.T_max) {
+                sm.out[i] = -1;  // padding (or an invalid entry that validation rejects)
+            } else if (s >= 0) {
+                sm.out[i] = s;
+                atomicOr(&sm.hitbits[s >> 5], 1u << (s & 31));
+                ++nhit;
+            } else {
+                sm.out[i] = -2;
+                missmask |= 1u << j;
+                ++nmiss;
+            }
+        }
+        uint32_t total;
+        const uint32_t excl = block_excl_scan(nmiss | (nhit << 16), &total, scan_sh);
+        m = (int)(total & 0xFFFFu);
+        h = (int)(total >> 16);
+        {
+            uint32_t o = excl & 0xFFFFu;
+#pragma unroll
+            for (int j = 0; j < kMaxIpt; ++j)
+                if (missmask & (1u << j))
+                    sm.miss[o++] = ((unsigned long long)(uint32_t)tok[j] << 32) | (uint32_t)(i0 + j);
+        }
+        __syncthreads();
+
+        // B. misses in ascending token order
+        int unsorted = 0;
+        for (int j = tid; j + 1 < m; j += NT)
+            if ((sm.miss[j] >> 32) > (sm.miss[j + 1] >> 32)) unsorted = 1;
+        if (__syncthreads_or(unsorted)) {
+            const int P = next_pow2(m);
+            for (int j = m + tid; j < P; j += NT) sm.miss[j] = ~0ull;
+            __syncthreads();
+            for (int size = 2; size <= P; size <<= 1) {
+                for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                    for (int i = tid; i < P / 2; i += NT) {
+                        const int lo = 2 * stride * (i / stride) + (i % stride), hi = lo + stride;
+                        const bool asc = (lo & size) == 0;
+                        const unsigned long long a = sm.miss[lo], c = sm.miss[hi];
+                        if ((a > c) == asc) {
+                            sm.miss[lo] = c;
+                            sm.miss[hi] = a;
+                        }
+                    }
+                    __syncthreads();
+                }
+            }
+        }
+
+        // the missing rows are known: start pulling (the first) of them over
+        // the host link while the LRU work below runs
+        {
+            const int npf = m < prefetch_rows ? m : prefetch_rows;
+            const uint8_t* src = d.pool + (size_t)u * d.T_max * d.row_bytes;
+            for (int j = tid; j < npf; j += NT)
+                prefetch_l2(src + (size_t)(sm.miss[j] >> 32) * d.row_bytes, (uint32_t)d.row_bytes);
+        }
+
+        // C. victims: the first m non-hit slots in LRU order
+        const int spt = (S + NT - 1) / NT;
+        const int p0 = tid * spt;
+        uint32_t cnt = 0;
+        for (int j = 0; j < spt; ++j) {
+            const int p = p0 + j;
+            if (p < S && !bit_test(sm.hitbits, sm.lru_old[p])) ++cnt;
+        }
+        uint32_t tot2;
+        uint32_t rank = block_excl_scan(cnt, &tot2, scan_sh);
+        for (int j = 0; j < spt; ++j) {
+            const int p = p0 + j;
+            if (p >= S) break;
+            const int s = sm.lru_old[p];
+            if (bit_test(sm.hitbits, s)) continue;
+            if ((int)rank < m) {
+                sm.victim[rank] = (uint16_t)s;
+                atomicOr(&sm.vicbits[s >> 5], 1u << (s & 31));
+            } else if ((int)rank - m < S) {
+                sm.lru_new[rank - m] = (uint16_t)s;
+            }
+            ++rank;
+        }
+        __syncthreads();
+
+        // D. the slots used by this step go to the back, by slot index
+        const int untouched = S - h - m;
+        uint32_t cnt3 = 0;
+        for (int j = 0; j < spt; ++j) {
+            const int s = p0 + j;
+            if (s < S && (bit_test(sm.hitbits, s) || bit_test(sm.vicbits, s))) ++cnt3;
+        }
+        uint32_t tot3;
+        uint32_t pos = block_excl_scan(cnt3, &tot3, scan_sh);
+        for (int j = 0; j < spt; ++j) {
+            const int s = p0 + j;
+            if (s < S && (bit_test(sm.hitbits, s) || bit_test(sm.vicbits, s)) && untouched + (int)pos < S && untouched >= 0)
+                sm.lru_new[untouched + pos++] = (uint16_t)s;
+        }
+    }
+
+    // nothing global has been written yet; from here on the call must be known valid
+    pdl_wait();
+    if (!r_ok || (d.ctl[CTL_ERR] | d.ctl[CTL_ERR_CALL]) != 0) {  // rejected call: -1 outputs, no state change
         for (int i = tid; i < k; i += NT) out[i] = -1;
         if (tid == 0) {
             hits_out[blockIdx.x] = -1;
@@ -284,132 +454,15 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Dev d, const int32_t
         if (kFused) finish_call(d);
         return;
     }
-
-    PlanSmem sm = carve_plan_smem(smem_raw, k, S);
-    const int b = blockIdx.x / d.L, l = blockIdx.x % d.L;
-    const int64_t u = (int64_t)req_ids[b] * d.L + l;
-    int32_t* t2s = d.tok2slot + u * d.T_max;
-    int32_t* s2t = d.slot2tok + u * S;
-    uint32_t* tsu = d.ts + u * S;
-    uint16_t* lru = d.lru + u * S;
     const uint32_t now1 = d.ctl[CTL_CLOCK] + 1u;
-    const int SW = (S + 31) / 32;
 
-    for (int w = tid; w < SW; w += NT) {
-        sm.hitbits[w] = 0u;
-        sm.vicbits[w] = 0u;
+    // E. stamps, map update and slot emission (plus gather jobs on the job-list path)
+    for (int i = tid; i < k; i += NT) {
+        const int32_t s = sm.out[i];
+        if (s >= 0) tsu[s] = now1;  // hit
     }
-    for (int p = tid; p < S; p += NT) sm.lru_old[p] = lru[p];
+    if (!kFused && tid == 0) job_base_sh = m ? atomicAdd(&d.ctl[CTL_JOBS], (uint32_t)m) : 0u;
     __syncthreads();
-
-    // A. sparse diff
-    const int ipt = (k + NT - 1) / NT;
-    const int i0 = tid * ipt;
-    int32_t tok[kMaxIpt];
-    uint32_t missmask = 0, nmiss = 0, nhit = 0;
-#pragma unroll
-    for (int j = 0; j < kMaxIpt; ++j) {
-        const int i = i0 + j;
-        tok[j] = -1;
-        if (j < ipt && i < k) {
-            const int32_t t = row[i];
-            tok[j] = t;
-            if (t >= 0) {
-                const int32_t s = t2s[t];
-                if (s >= 0) {
-                    sm.out[i] = s;
-                    atomicOr(&sm.hitbits[s >> 5], 1u << (s & 31));
-                    tsu[s] = now1;
-                    ++nhit;
-                } else {
-                    missmask |= 1u << j;
-                    ++nmiss;
-                }
-            } else {
-                sm.out[i] = -1;
-            }
-        }
-    }
-    uint32_t total;
-    const uint32_t excl = block_excl_scan(nmiss | (nhit << 16), &total, scan_sh);
-    const int m = (int)(total & 0xFFFFu), h = (int)(total >> 16);
-    {
-        uint32_t o = excl & 0xFFFFu;
-#pragma unroll
-        for (int j = 0; j < kMaxIpt; ++j)
-            if (missmask & (1u << j))
-                sm.miss[o++] = ((unsigned long long)(uint32_t)tok[j] << 32) | (uint32_t)(i0 + j);
-    }
-    __syncthreads();
-
-    // B. misses in ascending token order
-    int unsorted = 0;
-    for (int j = tid; j + 1 < m; j += NT)
-        if ((sm.miss[j] >> 32) > (sm.miss[j + 1] >> 32)) unsorted = 1;
-    if (__syncthreads_or(unsorted)) {
-        const int P = next_pow2(m);
-        for (int j = m + tid; j < P; j += NT) sm.miss[j] = ~0ull;
-        __syncthreads();
-        for (int size = 2; size <= P; size <<= 1) {
-            for (int stride = size >> 1; stride > 0; stride >>= 1) {
-                for (int i = tid; i < P / 2; i += NT) {
-                    const int lo = 2 * stride * (i / stride) + (i % stride), hi = lo + stride;
-                    const bool asc = (lo & size) == 0;
-                    const unsigned long long a = sm.miss[lo], c = sm.miss[hi];
-                    if ((a > c) == asc) {
-                        sm.miss[lo] = c;
-                        sm.miss[hi] = a;
-                    }
-                }
-                __syncthreads();
-            }
-        }
-    }
-
-    // C. victims: the first m non-hit slots in LRU order
-    const int spt = (S + NT - 1) / NT;
-    const int p0 = tid * spt;
-    uint32_t cnt = 0;
-    for (int j = 0; j < spt; ++j) {
-        const int p = p0 + j;
-        if (p < S && !bit_test(sm.hitbits, sm.lru_old[p])) ++cnt;
-    }
-    uint32_t tot2;
-    uint32_t rank = block_excl_scan(cnt, &tot2, scan_sh);
-    for (int j = 0; j < spt; ++j) {
-        const int p = p0 + j;
-        if (p >= S) break;
-        const int s = sm.lru_old[p];
-        if (bit_test(sm.hitbits, s)) continue;
-        if ((int)rank < m) {
-            sm.victim[rank] = (uint16_t)s;
-            atomicOr(&sm.vicbits[s >> 5], 1u << (s & 31));
-        } else {
-            sm.lru_new[rank - m] = (uint16_t)s;
-        }
-        ++rank;
-    }
-    __syncthreads();
-
-    // D. the slots used by this step go to the back, by slot index
-    const int untouched = S - h - m;
-    uint32_t cnt3 = 0;
-    for (int j = 0; j < spt; ++j) {
-        const int s = p0 + j;
-        if (s < S && (bit_test(sm.hitbits, s) || bit_test(sm.vicbits, s))) ++cnt3;
-    }
-    uint32_t tot3;
-    uint32_t pos = block_excl_scan(cnt3, &tot3, scan_sh);
-    for (int j = 0; j < spt; ++j) {
-        const int s = p0 + j;
-        if (s < S && (bit_test(sm.hitbits, s) || bit_test(sm.vicbits, s))) sm.lru_new[untouched + pos++] = (uint16_t)s;
-    }
-
-    // E. map update and slot emission (plus gather jobs on the job-list path)
-    if (!kFused) {
-        if (tid == 0) job_base_sh = m ? atomicAdd(&d.ctl[CTL_JOBS], (uint32_t)m) : 0u;
-        __syncthreads();
-    }
     for (int j = tid; j < m; j += NT) {
         const int v = sm.victim[j];
         const unsigned long long key = sm.miss[j];
@@ -426,7 +479,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Dev d, const int32_t
     __syncthreads();
 
     for (int i = tid; i < k; i += NT) out[i] = sm.out[i];
-    for (int p = tid; p < S; p += NT) lru[p] = sm.lru_new[p];
+    if ((S & 7) == 0) {
+        const uint4* src = reinterpret_cast<const uint4*>(sm.lru_new);
+        uint4* dst = reinterpret_cast<uint4*>(lru);
+        for (int p = tid; p < S / 8; p += NT) dst[p] = src[p];
+    } else {
+        for (int p = tid; p < S; p += NT) lru[p] = sm.lru_new[p];
+    }
     if (tid == 0) {
         hits_out[blockIdx.x] = h;
         misses_out[blockIdx.x] = m;
@@ -436,7 +495,6 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Dev d, const int32_t
 
     if (kFused) {
         // F. gather: pool row (u, token) -> hot row (u, victim slot)
-        const int cpr = CPR_CONST > 0 ? CPR_CONST : d.row_bytes / 16;
         const int4* __restrict__ src = reinterpret_cast<const int4*>(d.pool) + (size_t)u * d.T_max * cpr;
         int4* __restrict__ dst = reinterpret_cast<int4*>(d.hot) + (size_t)u * S * cpr;
         const int chunks = m * cpr;
@@ -566,22 +624,52 @@ cudaError_t launch_validate(const Dev& d, const int32_t* req_ids, int B, const i
 }
 
 cudaError_t launch_plan(const Dev& d, const int32_t* req_ids, int B, const int32_t* topk, int32_t* slots,
-                        int32_t* hits, int32_t* misses, cudaStream_t st)
+                        int32_t* hits, int32_t* misses, int prefetch_rows, bool pdl, cudaStream_t st)
 {
-    plan_kernel<false, 0>
-        <<<B * d.L, kPlanThreads, plan_smem_bytes(d.k, d.S), st>>>(d, req_ids, topk, slots, hits, misses);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(B * d.L);
+    cfg.blockDim = dim3(kPlanThreads);
+    cfg.dynamicSmemBytes = plan_smem_bytes(d.k, d.S);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, plan_kernel<false, 0>, d, req_ids, topk, slots, hits, misses, prefetch_rows);
 }
 
 cudaError_t launch_plan_gather(const Dev& d, const int32_t* req_ids, int B, const int32_t* topk, int32_t* slots,
-                               int32_t* hits, int32_t* misses, cudaStream_t st)
+                               int32_t* hits, int32_t* misses, int resident_ctas, cudaStream_t st)
 {
-    const size_t smem = plan_smem_bytes(d.k, d.S);
+    // L2 prefetch budget: half of L2 shared by the CTAs that can be resident at once
+    const int grid = B * d.L;
+    const int concurrent = grid < resident_ctas ? grid : (resident_ctas > 0 ? resident_ctas : 1);
+    const int prefetch_rows = (int)((kPrefetchBudgetBytes / d.row_bytes) / concurrent);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kPlanThreads);
+    cfg.dynamicSmemBytes = plan_smem_bytes(d.k, d.S);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (d.row_bytes == 1152)
-        plan_kernel<true, 72><<<B * d.L, kPlanThreads, smem, st>>>(d, req_ids, topk, slots, hits, misses);
-    else
-        plan_kernel<true, 0><<<B * d.L, kPlanThreads, smem, st>>>(d, req_ids, topk, slots, hits, misses);
-    return cudaGetLastError();
+        return cudaLaunchKernelEx(&cfg, plan_kernel<true, 72>, d, req_ids, topk, slots, hits, misses, prefetch_rows);
+    return cudaLaunchKernelEx(&cfg, plan_kernel<true, 0>, d, req_ids, topk, slots, hits, misses, prefetch_rows);
+}
+
+int plan_resident_ctas(int k, int S)
+{
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, plan_kernel<true, 72>, kPlanThreads,
+                                                      plan_smem_bytes(k, S)) != cudaSuccess)
+        return 1;
+    return sms * (per_sm > 0 ? per_sm : 1);
 }
 
 cudaError_t launch_gather(const Dev& d, int grid, cudaStream_t st)
