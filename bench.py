@@ -192,8 +192,8 @@ def hbm_peak_gbs():
 # dram__bytes_read.sum + dram__bytes_write.sum.  Valid only while the kernel
 # source is the one that was captured; scaled to other workloads by units.
 PROFILED_TRAFFIC = {"source": "sparse_attention_kv_skv_gb300/csrc/skv_step_kernels.cu",
-                    "sha256": "f3ae9416066b64aaef853af5f4170d6cb3ebf50f72a3e8b0a6143717e2713529",
-                    "units": 512, "dram_bytes": 42.706432e6 + 194.308096e6,
+                    "sha256": "2dac0a375f4b917a2b98899aea467649508f7c79d30459126d9488e6b5cc0619",
+                    "units": 512, "dram_bytes": 42.669312e6 + 200.168192e6,
                     "summary": "profiles/plan_gather_kernel_c2_16k_b64.md"}
 
 

@@ -354,6 +354,10 @@ __global__ void __launch_bounds__(kPlanThreads, 3) plan_kernel(Dev d, const int3
                 sm.out[i] = -2;
                 missmask |= 1u << j;
                 ++nmiss;
+                // the budget covers every possible miss of this unit: start
+                // pulling the row over the host link right away
+                if (prefetch_rows >= k)
+                    prefetch_l2(d.pool + ((size_t)u * d.T_max + t) * d.row_bytes, (uint32_t)d.row_bytes);
             }
         }
         uint32_t total;
@@ -395,7 +399,7 @@ __global__ void __launch_bounds__(kPlanThreads, 3) plan_kernel(Dev d, const int3
 
         // the missing rows are known: start pulling (the first) of them over
         // the host link while the LRU work below runs
-        {
+        if (prefetch_rows < k) {  // otherwise every row was prefetched in phase A
             const int npf = m < prefetch_rows ? m : prefetch_rows;
             const uint8_t* src = d.pool + (size_t)u * d.T_max * d.row_bytes;
             for (int j = tid; j < npf; j += NT)
@@ -642,10 +646,12 @@ cudaError_t launch_plan(const Dev& d, const int32_t* req_ids, int B, const int32
 cudaError_t launch_plan_gather(const Dev& d, const int32_t* req_ids, int B, const int32_t* topk, int32_t* slots,
                                int32_t* hits, int32_t* misses, int resident_ctas, cudaStream_t st)
 {
-    // L2 prefetch budget: half of L2 shared by the CTAs that can be resident at once
+    // L2 prefetch of the missing rows pays only when every CTA is resident at
+    // once (few units: planning is otherwise exposed); with more units than
+    // fit, the link is already kept busy by other CTAs and the prefetched
+    // lines compete with the streaming gather (measured: -1.5 % to -4 %)
     const int grid = B * d.L;
-    const int concurrent = grid < resident_ctas ? grid : (resident_ctas > 0 ? resident_ctas : 1);
-    const int prefetch_rows = (int)((kPrefetchBudgetBytes / d.row_bytes) / concurrent);
+    const int prefetch_rows = grid <= resident_ctas ? (int)((kPrefetchBudgetBytes / d.row_bytes) / grid) : 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kPlanThreads);
