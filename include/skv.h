@@ -171,6 +171,26 @@ SKV_API skv_status skv_write_back(skv_ctx *ctx, const int32_t *req_ids_dev, int3
 SKV_API skv_status skv_assemble(skv_ctx *ctx, const int32_t *req_ids_dev, int32_t B, const int32_t *topk_dev,
                         int32_t *slots_dev, int32_t *hits_dev, int32_t *misses_dev, skv_stream_t stream);
 
+/* skv_assemble for one layer only: for each batch entry b < B, make every
+ * token of topk_dev[b][0..k) resident in the hot buffer of request
+ * req_ids_dev[b], layer `layer`, and write its slot to slots_dev[b][i]
+ * (hits_dev / misses_dev are [B]).  Other layers are untouched.  A decode
+ * step can thus assemble layer by layer, as each layer's Top-k becomes known,
+ * and overlap layer l+1's transfer with other work on another stream (the
+ * pages: on-demand assembly of the data the current computation needs, its
+ * data-movement overhead and HiSparse's prefetching -- "Sparse
+ * Attention-Driven KVCache Management for Domestic AI Supernodes", abstract
+ * and agenda item 3; "XM-Sparse: Netpreme X-Mem ...", section
+ * "与SGLang HiSparse的集成").  Same validation, errors and output conventions as
+ * skv_assemble; every successful call advances the step clock by one, so the
+ * replacement order within a (request, layer) is the order of the calls that
+ * touched it.  Calls on one context must still be ordered (one stream), since
+ * they share the control words; the overlap is with the caller's other work.
+ * SKV_ERR_INVALID_ARG if layer is outside [0, L).  Captures into a CUDA graph. */
+SKV_API skv_status skv_assemble_layer(skv_ctx *ctx, const int32_t *req_ids_dev, int32_t B, int32_t layer,
+                                      const int32_t *topk_dev, int32_t *slots_dev, int32_t *hits_dev,
+                                      int32_t *misses_dev, skv_stream_t stream);
+
 /* skv_assemble for callers whose per-step tensors live in host memory
  * (pinned or pageable): copies req_ids [B] and topk [B][L][k] to device
  * staging buffers owned by the context, runs skv_assemble, copies slots, hits

@@ -63,6 +63,8 @@ def load(path: str | None = None):
     L.orc_write_back.argtypes = [vp, vp, i32, vp]
     L.orc_assemble.restype = i32
     L.orc_assemble.argtypes = [vp, vp, i32, vp, vp, vp, vp, i32]
+    L.orc_assemble_layer.restype = i32
+    L.orc_assemble_layer.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp, i32]
     L.orc_get_error.restype = i32
     L.orc_get_error.argtypes = [vp]
     L.orc_now.restype = u32
@@ -146,6 +148,18 @@ class Oracle:
         misses = np.empty((B, self.L), dtype=np.int32)
         err = self.lib.orc_assemble(self.h, _ptr(req), B, _ptr(topk), _ptr(slots), _ptr(hits), _ptr(misses),
                                     nthreads)
+        return int(err), slots, hits, misses
+
+    def assemble_layer(self, layer: int, req_ids, topk: np.ndarray, nthreads: int = 1):
+        """One layer: topk [B][k] -> (err, slots[B][k], hits[B], misses[B])."""
+        req = np.ascontiguousarray(np.asarray(req_ids, dtype=np.int32))
+        B = req.size
+        topk = np.ascontiguousarray(topk, dtype=np.int32).reshape(B, self.k)
+        slots = np.empty_like(topk)
+        hits = np.empty(B, dtype=np.int32)
+        misses = np.empty(B, dtype=np.int32)
+        err = self.lib.orc_assemble_layer(self.h, _ptr(req), B, layer, _ptr(topk), _ptr(slots), _ptr(hits),
+                                          _ptr(misses), nthreads)
         return int(err), slots, hits, misses
 
     def get_error(self) -> int:

@@ -241,20 +241,20 @@ int32_t orc_write_back(void* h, const int32_t* req_ids, int32_t n, const uint8_t
     return 0;
 }
 
-// One decode step: topk is [B][L][k]; slots (same shape) receives slot indices
-// (-1 for -1 entries); hits / misses are [B][L].  Returns the error bits of
-// this call, or the already-set sticky word; on any error the outputs are -1
-// and nothing else changes.
-int32_t orc_assemble(void* h, const int32_t* req_ids, int32_t B, const int32_t* topk, int32_t* slots,
-                     int32_t* hits, int32_t* misses, int32_t nthreads)
+// One decode step over the units of `layers` (all L layers when layer < 0,
+// else only that layer): topk is [B][nl][k] with nl = L or 1; slots (same
+// shape) receives slot indices (-1 for -1 entries); hits / misses are
+// [B][nl].  Returns the error bits of this call, or the already-set sticky
+// word; on any error the outputs are -1 and nothing else changes.
+static int32_t assemble_units(Oracle* o, const int32_t* req_ids, int32_t B, int32_t layer, const int32_t* topk,
+                              int32_t* slots, int32_t* hits, int32_t* misses, int32_t nthreads)
 {
-    Oracle* o = static_cast<Oracle*>(h);
-    const int64_t L = o->L, k = o->k;
+    const int64_t nl = layer < 0 ? o->L : 1, k = o->k;
     if (B <= 0) return 0;
     auto reject = [&]() {
-        std::fill(slots, slots + (size_t)B * L * k, -1);
-        std::fill(hits, hits + (size_t)B * L, -1);
-        std::fill(misses, misses + (size_t)B * L, -1);
+        std::fill(slots, slots + (size_t)B * nl * k, -1);
+        std::fill(hits, hits + (size_t)B * nl, -1);
+        std::fill(misses, misses + (size_t)B * nl, -1);
     };
     if (o->err) {
         reject();
@@ -271,9 +271,9 @@ int32_t orc_assemble(void* h, const int32_t* req_ids, int32_t B, const int32_t* 
         }
         if (!seen.insert(r).second) e |= E_BAD_REQUEST;
         const int64_t len = o->req[r].len;
-        for (int64_t l = 0; l < L; ++l) {
+        for (int64_t j = 0; j < nl; ++j) {
             std::unordered_set<int32_t> row_tokens;
-            const int32_t* row = topk + ((size_t)b * L + l) * k;
+            const int32_t* row = topk + ((size_t)b * nl + j) * k;
             for (int64_t i = 0; i < k; ++i) {
                 const int32_t t = row[i];
                 if (t == -1) continue;
@@ -288,15 +288,34 @@ int32_t orc_assemble(void* h, const int32_t* req_ids, int32_t B, const int32_t* 
         return e;
     }
     const uint32_t now = o->now + 1;
-    const int64_t units = (int64_t)B * L;
+    const int64_t units = (int64_t)B * nl;
     if (nthreads < 1) nthreads = 1;
 #pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
     for (int64_t x = 0; x < units; ++x) {
-        const int32_t b = (int32_t)(x / L), l = (int32_t)(x % L);
+        const int32_t b = (int32_t)(x / nl);
+        const int32_t l = layer < 0 ? (int32_t)(x % nl) : layer;
         assemble_unit(o, req_ids[b], l, topk + x * k, slots + x * k, hits + x, misses + x, now);
     }
     o->now = now;
     return 0;
+}
+
+// One decode step over all layers: topk is [B][L][k].
+int32_t orc_assemble(void* h, const int32_t* req_ids, int32_t B, const int32_t* topk, int32_t* slots,
+                     int32_t* hits, int32_t* misses, int32_t nthreads)
+{
+    return assemble_units(static_cast<Oracle*>(h), req_ids, B, -1, topk, slots, hits, misses, nthreads);
+}
+
+// One step of one layer: topk is [B][k]; the clock advances by one as for a
+// full step, so the replacement order of a (request, layer) follows the order
+// of the calls that touched it.  Returns -100 for a layer outside [0, L).
+int32_t orc_assemble_layer(void* h, const int32_t* req_ids, int32_t B, int32_t layer, const int32_t* topk,
+                           int32_t* slots, int32_t* hits, int32_t* misses, int32_t nthreads)
+{
+    Oracle* o = static_cast<Oracle*>(h);
+    if (layer < 0 || layer >= o->L) return -100;
+    return assemble_units(o, req_ids, B, layer, topk, slots, hits, misses, nthreads);
 }
 
 // Read and clear the sticky error word.

@@ -43,7 +43,11 @@ struct Dev {
     unsigned long long* stats;  // [STAT_WORDS]
     uint2* jobs;           // gather work list: (source pool row, destination hot row)
     int64_t* wb_pos;       // [max_batch] write-back target positions
+    int32_t layer_sel;     // -1: a call covers all L layers (CTA = b*L + l); else only this layer (CTA = b)
 };
+
+// CTAs (units) of one assemble call.
+inline int call_units(const Dev& d, int B) { return d.layer_sel >= 0 ? B : B * d.L; }
 
 // Shared-memory bytes the plan kernel needs for (k, S).
 size_t plan_smem_bytes(int k, int S);

@@ -188,6 +188,7 @@ skv_status skv_create(const skv_config* cfg, skv_ctx** out)
     d.S = c.hot_slots;
     d.row_bytes = c.row_bytes;
     d.T_max = c.max_context;
+    d.layer_sel = -1;
 
     auto fail = [&](cudaError_t e, const char* what) {
         skv_status s = (e == cudaErrorMemoryAllocation) ? SKV_ERR_OOM : cuda_fail(e, what);
@@ -304,6 +305,25 @@ skv_status skv_write_back(skv_ctx* ctx, const int32_t* req_ids_dev, int32_t n, c
     return SKV_OK;
 }
 
+}  // extern "C"
+
+namespace {
+// The launch sequence of one assemble call over the units described by `d`
+// (all layers, or the one in d.layer_sel).
+skv_status assemble_impl(skv_ctx* ctx, const Dev& d, const int32_t* req_ids_dev, int32_t B, const int32_t* topk_dev,
+                         int32_t* slots_dev, int32_t* hits_dev, int32_t* misses_dev, cudaStream_t stream)
+{
+    SKV_CUDA(skv::launch_validate(d, req_ids_dev, B, topk_dev, stream));
+    if (ctx->ev_before) SKV_CUDA(record_event(ctx->ev_before, stream));
+    SKV_CUDA(skv::launch_plan_gather(d, req_ids_dev, B, topk_dev, slots_dev, hits_dev, misses_dev, ctx->plan_resident,
+                                     stream));
+    if (ctx->ev_after) SKV_CUDA(record_event(ctx->ev_after, stream));
+    return SKV_OK;
+}
+}  // namespace
+
+extern "C" {
+
 skv_status skv_assemble(skv_ctx* ctx, const int32_t* req_ids_dev, int32_t B, const int32_t* topk_dev,
                         int32_t* slots_dev, int32_t* hits_dev, int32_t* misses_dev, skv_stream_t stream)
 {
@@ -311,13 +331,21 @@ skv_status skv_assemble(skv_ctx* ctx, const int32_t* req_ids_dev, int32_t B, con
     if (B == 0) return SKV_OK;
     if (!req_ids_dev || !topk_dev || !slots_dev || !hits_dev || !misses_dev) return SKV_ERR_INVALID_ARG;
     DeviceGuard g(ctx->cfg.device);
-    const Dev& d = ctx->d;
-    SKV_CUDA(skv::launch_validate(d, req_ids_dev, B, topk_dev, stream));
-    if (ctx->ev_before) SKV_CUDA(record_event(ctx->ev_before, stream));
-    SKV_CUDA(skv::launch_plan_gather(d, req_ids_dev, B, topk_dev, slots_dev, hits_dev, misses_dev, ctx->plan_resident,
-                                     stream));
-    if (ctx->ev_after) SKV_CUDA(record_event(ctx->ev_after, stream));
-    return SKV_OK;
+    return assemble_impl(ctx, ctx->d, req_ids_dev, B, topk_dev, slots_dev, hits_dev, misses_dev, stream);
+}
+
+skv_status skv_assemble_layer(skv_ctx* ctx, const int32_t* req_ids_dev, int32_t B, int32_t layer,
+                              const int32_t* topk_dev, int32_t* slots_dev, int32_t* hits_dev, int32_t* misses_dev,
+                              skv_stream_t stream)
+{
+    if (!ctx || B < 0 || B > ctx->cfg.max_batch || layer < 0 || layer >= ctx->cfg.num_layers)
+        return SKV_ERR_INVALID_ARG;
+    if (B == 0) return SKV_OK;
+    if (!req_ids_dev || !topk_dev || !slots_dev || !hits_dev || !misses_dev) return SKV_ERR_INVALID_ARG;
+    DeviceGuard g(ctx->cfg.device);
+    Dev d = ctx->d;
+    d.layer_sel = layer;
+    return assemble_impl(ctx, d, req_ids_dev, B, topk_dev, slots_dev, hits_dev, misses_dev, stream);
 }
 
 skv_status skv_assemble_host(skv_ctx* ctx, const int32_t* req_ids, int32_t B, const int32_t* topk, int32_t* slots,

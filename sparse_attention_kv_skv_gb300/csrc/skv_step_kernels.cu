@@ -111,14 +111,15 @@ __global__ void __launch_bounds__(kValidateThreads) validate_kernel(Dev d, const
     pdl_launch_dependents();  // the plan kernel may start its read-only work now
     if (blockIdx.x == 0 && threadIdx.x == 0) d.ctl[CTL_JOBS] = 0;
     if (d.ctl[CTL_ERR] != 0) return;  // sticky error: the call is a no-op
-    const int b = blockIdx.x / d.L, l = blockIdx.x % d.L;
+    const int b = d.layer_sel >= 0 ? (int)blockIdx.x : (int)blockIdx.x / d.L;
+    const int l = d.layer_sel >= 0 ? d.layer_sel : (int)blockIdx.x % d.L;
     const int32_t r = req_ids[b];
     if (r < 0 || r >= d.R || d.active[r] == 0) {
         if (threadIdx.x == 0) atomicOr(&d.ctl[CTL_ERR_CALL], DEVERR_BAD_REQUEST);
         return;  // uniform across the CTA
     }
     uint32_t f = 0;
-    if (l == 0)
+    if (d.layer_sel >= 0 || l == 0)  // one CTA per batch entry compares its id with the earlier ones
         for (int j = threadIdx.x; j < b; j += blockDim.x)
             if (req_ids[j] == r) f |= DEVERR_BAD_REQUEST;
     if (threadIdx.x == 0) flags = 0;
@@ -300,7 +301,8 @@ __global__ void __launch_bounds__(kPlanThreads, 3) plan_kernel(Dev d, const int3
     int32_t* out = slots_out + (size_t)blockIdx.x * k;
 
     PlanSmem sm = carve_plan_smem(smem_raw, k, S);
-    const int b = blockIdx.x / d.L, l = blockIdx.x % d.L;
+    const int b = d.layer_sel >= 0 ? (int)blockIdx.x : (int)blockIdx.x / d.L;
+    const int l = d.layer_sel >= 0 ? d.layer_sel : (int)blockIdx.x % d.L;
     const int32_t r = req_ids[b];
     const bool r_ok = r >= 0 && r < d.R;  // uniform over the CTA; validation decides the rest
     const int64_t u = (int64_t)(r_ok ? r : 0) * d.L + l;
@@ -623,7 +625,7 @@ cudaError_t prepare_step_kernels(int k, int S, int* gather_grid)
 cudaError_t launch_validate(const Dev& d, const int32_t* req_ids, int B, const int32_t* topk, cudaStream_t st)
 {
     const int lg = table_log2_for(d.k);
-    validate_kernel<<<B * d.L, kValidateThreads, validate_smem_bytes(d.k), st>>>(d, req_ids, B, topk, lg);
+    validate_kernel<<<call_units(d, B), kValidateThreads, validate_smem_bytes(d.k), st>>>(d, req_ids, B, topk, lg);
     return cudaGetLastError();
 }
 
@@ -631,7 +633,7 @@ cudaError_t launch_plan(const Dev& d, const int32_t* req_ids, int B, const int32
                         int32_t* hits, int32_t* misses, int prefetch_rows, bool pdl, cudaStream_t st)
 {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(B * d.L);
+    cfg.gridDim = dim3(call_units(d, B));
     cfg.blockDim = dim3(kPlanThreads);
     cfg.dynamicSmemBytes = plan_smem_bytes(d.k, d.S);
     cfg.stream = st;
@@ -650,7 +652,7 @@ cudaError_t launch_plan_gather(const Dev& d, const int32_t* req_ids, int B, cons
     // once (few units: planning is otherwise exposed); with more units than
     // fit, the link is already kept busy by other CTAs and the prefetched
     // lines compete with the streaming gather (measured: -1.5 % to -4 %)
-    const int grid = B * d.L;
+    const int grid = call_units(d, B);
     const int prefetch_rows = grid <= resident_ctas ? (int)((kPrefetchBudgetBytes / d.row_bytes) / grid) : 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);

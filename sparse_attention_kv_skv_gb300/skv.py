@@ -60,6 +60,7 @@ def _load():
         "skv_assemble": [vp, vp, i32, vp, vp, vp, vp, vp],
         "skv_assemble_host": [vp, vp, i32, vp, vp, vp, vp, vp],
         "skv_assemble_noalloc": [vp, vp, i32, vp, vp, vp, vp, vp],
+        "skv_assemble_layer": [vp, vp, i32, i32, vp, vp, vp, vp, vp],
         "skv_release": [vp, i32, vp],
         "skv_get_device_error": [vp, P(i32), vp],
         "skv_hot_buffer": [vp, P(vp), P(i64)],
@@ -91,6 +92,7 @@ skv_write_back = lib.skv_write_back
 skv_assemble = lib.skv_assemble
 skv_assemble_host = lib.skv_assemble_host
 skv_assemble_noalloc = lib.skv_assemble_noalloc
+skv_assemble_layer = lib.skv_assemble_layer
 skv_release = lib.skv_release
 skv_get_device_error = lib.skv_get_device_error
 skv_hot_buffer = lib.skv_hot_buffer
@@ -199,6 +201,13 @@ class Context:
         B = req_ids.numel() if B is None else B
         check(skv_assemble(self.h, _ptr(req_ids), B, _ptr(topk), _ptr(slots), _ptr(hits), _ptr(misses),
                            _stream_handle(stream)), "skv_assemble")
+
+    def assemble_layer(self, layer: int, req_ids, topk, slots, hits, misses, B: int | None = None,
+                       stream=None) -> None:
+        """One layer's assemble: topk / slots are [B][k], hits / misses [B]."""
+        B = req_ids.numel() if B is None else B
+        check(skv_assemble_layer(self.h, _ptr(req_ids), B, layer, _ptr(topk), _ptr(slots), _ptr(hits),
+                                 _ptr(misses), _stream_handle(stream)), "skv_assemble_layer")
 
     def assemble_noalloc(self, req_ids, topk, slots, hits, misses, B: int | None = None, stream=None) -> None:
         """skv_assemble with the gather work list in the library's static

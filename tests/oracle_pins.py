@@ -408,3 +408,59 @@ def check_errors(lib_path=None):
     assert (st["slot2tok"] == -1).all() and (st["ts"] == 0).all() and st["len"] == T
     assert not o.export_hot(0).any()
     o.close()
+
+
+# ----------------------------------------------------------------------------
+# one-layer steps against full steps
+# ----------------------------------------------------------------------------
+
+def check_layer_mode(lib_path=None, steps=6):
+    """Assembling layers 0..L-1 one call each must leave every (request, layer)
+    exactly as one call over all layers does -- same slots, counts, maps, LRU
+    order and bytes -- except that the clock advances once per call, so a slot
+    stamped c by the full call (c = step + 1) is stamped (c - 1) * L + l + 1 by
+    the layer calls."""
+    w = wl.Workload("layers", B=3, L=3, ctx=400, k=24, S=40, steps=steps, fresh=0.4, order=wl.ORDER_SHUFFLED,
+                    n_pad=3)
+    pool = make_pool(w.B, w.L, w.ctx, seed=21)
+    full = orc.Oracle(w.B, w.L, w.ctx, RB, w.k, w.S, pool, lib_path=lib_path)
+    per = orc.Oracle(w.B, w.L, w.ctx, RB, w.k, w.S, pool, lib_path=lib_path)
+    for _ in range(w.B):
+        full.publish(w.ctx)
+        per.publish(w.ctx)
+    req = [2, 0, 1]
+    gen = wl.TopkStream(w, nthreads=1)
+    for s in range(steps):
+        topk = gen.step(s, [w.ctx] * w.B)
+        e, slots, hits, misses = full.assemble(req, topk)
+        assert e == 0
+        for l in range(w.L):
+            e, sl, h, m = per.assemble_layer(l, req, topk[:, l, :])
+            assert e == 0
+            assert np.array_equal(sl, slots[:, l, :]), (s, l)
+            assert np.array_equal(h, hits[:, l]) and np.array_equal(m, misses[:, l]), (s, l)
+    assert per.now == steps * w.L and full.now == steps
+    for r in range(w.B):
+        a, b = full.export(r), per.export(r)
+        for key in ("slot2tok", "tok2slot", "lru"):
+            assert np.array_equal(a[key], b[key]), (r, key)
+        for l in range(w.L):
+            ts_a = a["ts"][l].astype(np.int64)
+            want = np.where(ts_a > 0, (ts_a - 1) * w.L + l + 1, 0)
+            assert np.array_equal(b["ts"][l], want), (r, l)
+        assert np.array_equal(full.export_hot(r), per.export_hot(r)), r
+    # a bad layer is refused; an error in one layer's call changes nothing
+    assert per.assemble_layer(w.L, req, topk[:, 0, :])[0] == -100
+    before = [per.export(r) for r in range(w.B)]
+    bad = topk[:, 1, :].copy()
+    bad[1, 0] = w.ctx
+    e, sl, h, m = per.assemble_layer(1, req, bad)
+    assert e == orc.E_BAD_INDEX and (sl == -1).all() and (h == -1).all()
+    assert per.get_error() == orc.E_BAD_INDEX
+    for r in range(w.B):
+        after = per.export(r)
+        for key in ("slot2tok", "ts", "lru"):
+            assert np.array_equal(before[r][key], after[key])
+    full.close()
+    per.close()
+    gen.close()

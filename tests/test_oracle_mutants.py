@@ -8,13 +8,16 @@ no such mistake could hide behind the current pins.
 """
 import concurrent.futures as cf
 import os
+import subprocess
+import sys
 import tempfile
 
 import pytest
 
 import oracle as orc
-import skv_workload as wl
-import oracle_pins as pins
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
 
 MUTANTS = {
     "tie_break_highest_slot": [
@@ -47,6 +50,12 @@ MUTANTS = {
          "victims.push_back(u.lru.back());\n        u.lru.pop_back();")],
     "write_back_no_len_increment": [
         ("        q.len += 1;\n", "")],
+    "layer_index_ignored": [
+        ("const int32_t l = layer < 0 ? (int32_t)(x % nl) : layer;",
+         "const int32_t l = layer < 0 ? (int32_t)(x % nl) : 0;")],
+    "layer_call_not_validated": [
+        ("for (int64_t j = 0; j < nl; ++j) {\n            std::unordered_set<int32_t> row_tokens;",
+         "for (int64_t j = 0; j < (layer < 0 ? nl : 0); ++j) {\n            std::unordered_set<int32_t> row_tokens;")],
     "sticky_error_ignored": [
         ("    if (o->err) {\n        reject();\n        return o->err;\n    }", "")],
 }
@@ -62,28 +71,43 @@ def _build(name, edits, tmp):
     return orc.compile_oracle(p, os.path.join(tmp, f"lib{name}.so"))
 
 
+_CHECKS = """
+import sys
+import oracle_pins as pins, skv_workload as wl
+lib = sys.argv[1]
+checks = [
+    lambda: pins.check_golden(lib),
+    lambda: pins.check_closed_forms(lib),
+    lambda: pins.check_errors(lib),
+    lambda: pins.check_bruteforce(lib, T=4, k=2, S_values=(2, 3), steps=3, variant="ordered"),
+    lambda: pins.check_invariants(wl.Workload("mut_inv", B=2, L=1, ctx=100, k=12, S=20, steps=6, fresh=0.4,
+                                              order=wl.ORDER_SHUFFLED), lib),
+    lambda: pins.check_layer_mode(lib, steps=3),
+]
+for c in checks:
+    try:
+        c()
+    except (AssertionError, IndexError, KeyError, ValueError):
+        sys.exit(1)
+sys.exit(0)
+"""
+
+
 def _caught(lib_path):
-    checks = [
-        lambda: pins.check_golden(lib_path),
-        lambda: pins.check_closed_forms(lib_path),
-        lambda: pins.check_errors(lib_path),
-        lambda: pins.check_bruteforce(lib_path, T=4, k=2, S_values=(2, 3), steps=3, variant="ordered"),
-        lambda: pins.check_invariants(wl.Workload("mut_inv", B=2, L=1, ctx=100, k=12, S=20, steps=6, fresh=0.4,
-                                                  order=wl.ORDER_SHUFFLED), lib_path),
-    ]
-    for c in checks:
-        try:
-            c()
-        except (AssertionError, IndexError, KeyError, ValueError):
-            return True
-    return False
+    """Run every pin on the library in a child process; a failed pin or a crash
+    (a mistake can make the oracle throw or read out of bounds) counts as caught."""
+    env = dict(os.environ, PYTHONPATH=os.pathsep.join([ROOT, HERE, os.environ.get("PYTHONPATH", "")]))
+    p = subprocess.run([sys.executable, "-c", _CHECKS, lib_path], env=env, capture_output=True, timeout=600)
+    return p.returncode != 0
 
 
 def test_every_planted_mistake_is_caught():
     with tempfile.TemporaryDirectory() as tmp:
         with cf.ThreadPoolExecutor(max_workers=os.cpu_count() or 2) as ex:
             libs = dict(zip(MUTANTS, ex.map(lambda kv: _build(kv[0], kv[1], tmp), MUTANTS.items())))
-        missed = [name for name, lib in libs.items() if not _caught(lib)]
+        with cf.ThreadPoolExecutor(max_workers=os.cpu_count() or 2) as ex:
+            caught = dict(zip(libs, ex.map(_caught, libs.values())))
+        missed = [name for name, c in caught.items() if not c]
     assert not missed, f"pins did not catch: {missed}"
 
 

@@ -44,3 +44,7 @@ def test_invariants(w):
 
 def test_errors_and_lifecycle():
     pins.check_errors()
+
+
+def test_layer_calls_match_full_steps():
+    pins.check_layer_mode()
