@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wl.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of per-step CUDA graphs")
+    ap.add_argument("--layered", action="store_true",
+                    help="each step assembles layer by layer (L skv_assemble_layer calls) instead of one call")
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--cpu-sample-requests", type=int, default=32)
     ap.add_argument("--cpu-sample-steps", type=int, default=24)
@@ -293,33 +295,55 @@ def run_ours(args):
     gen = wl.TopkStream(w)
     lens = [w.ctx] * w.B
     n_dev = W + K
-    topk_all = torch.empty((n_dev, w.B, w.L, w.k), dtype=torch.int32, device=dev)
+    layered = args.layered
+    per_call = w.L if layered else 1  # assemble calls per step
+    # per step: [B][L][k] for one call, or layer-major [L][B][k] for layer calls
+    topk_all = torch.empty((n_dev, w.L, w.B, w.k) if layered else (n_dev, w.B, w.L, w.k), dtype=torch.int32,
+                           device=dev)
     wb_rows = None
     host_steps = []
     for s in range(n_dev + args.e2e_steps):
-        x = gen.step(s, [l + (s if w.appends else 0) for l in lens])
+        x = gen.step(s, [w.len_at(s)] * w.B)
         if s < n_dev:
-            topk_all[s].copy_(torch.from_numpy(x))
+            topk_all[s].copy_(torch.from_numpy(np.ascontiguousarray(x.transpose(1, 0, 2)) if layered else x))
         else:
             host_steps.append(torch.from_numpy(x).pin_memory())
     if w.appends:
         # the appended rows' contents do not affect timing: one fixed block per step
         wb_rows = torch.zeros((w.B, w.L, rb), dtype=torch.uint8, device=dev)
+    ext_rows = None
+    if w.turn_every:
+        # a new turn of every session: turn_tokens more rows per layer (skv_extend)
+        ext_rows = torch.zeros((w.L, w.turn_tokens, rb), dtype=torch.uint8, device=dev)
+
+    def new_turn(s):
+        return w.turn_every and s > 0 and s % w.turn_every == 0
     req = torch.arange(w.B, dtype=torch.int32, device=dev)
-    slots = torch.empty((w.B, w.L, w.k), dtype=torch.int32, device=dev)
-    hits = torch.empty((n_dev, w.B, w.L), dtype=torch.int32, device=dev)
-    misses = torch.empty((n_dev, w.B, w.L), dtype=torch.int32, device=dev)
+    slots = torch.empty((w.L, w.B, w.k) if layered else (w.B, w.L, w.k), dtype=torch.int32, device=dev)
+    hits = torch.empty((n_dev, w.L, w.B) if layered else (n_dev, w.B, w.L), dtype=torch.int32, device=dev)
+    misses = torch.empty_like(hits)
     stream = torch.cuda.Stream(device=dev)
-    ev_b = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n_dev)]
-    ev_a = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n_dev)]
+    n_ev = n_dev * (w.L if layered else 1)  # one pair per assemble call
+    ev_b = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n_ev)]
+    ev_a = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n_ev)]
     for ev in ev_b + ev_a:  # torch creates the CUDA event lazily, at its first record
         ev.record(stream)
     torch.cuda.synchronize()
     assert all(ev.cuda_event for ev in ev_b + ev_a)
 
     def enqueue(s):
-        ctx.set_gather_events(ev_b[s], ev_a[s])
-        ctx.assemble(req, topk_all[s], slots, hits[s], misses[s], stream=stream.cuda_stream)
+        if new_turn(s):
+            for r in range(w.B):
+                ctx.extend(r, ext_rows, w.turn_tokens, stream=stream.cuda_stream)
+        if layered:
+            for l in range(w.L):
+                e = s * w.L + l
+                ctx.set_gather_events(ev_b[e], ev_a[e])
+                ctx.assemble_layer(l, req, topk_all[s, l], slots[l], hits[s, l], misses[s, l],
+                                   stream=stream.cuda_stream)
+        else:
+            ctx.set_gather_events(ev_b[s], ev_a[s])
+            ctx.assemble(req, topk_all[s], slots, hits[s], misses[s], stream=stream.cuda_stream)
         if w.appends:
             ctx.write_back(req, wb_rows, stream=stream.cuda_stream)
 
@@ -366,9 +390,9 @@ def run_ours(args):
     st1 = ctx.stats()
     M = st1["misses"] - st0["misses"]
     H = st1["hits"] - st0["hits"]
-    assert st1["calls"] - st0["calls"] == K
+    assert st1["calls"] - st0["calls"] == K * per_call
     assert ctx.get_device_error() == 0
-    gather_s = sum(event_ms(ev_b[s], ev_a[s]) for s in range(W, n_dev)) / 1e3
+    gather_s = sum(event_ms(ev_b[e], ev_a[e]) for e in range(W * per_call, n_dev * per_call)) / 1e3
     per_step_m = misses[W:].sum(dim=(1, 2)).cpu().numpy().astype(np.int64)
     per_step_h = hits[W:].sum(dim=(1, 2)).cpu().numpy().astype(np.int64)
     assert int(per_step_m.sum()) == M
@@ -389,7 +413,10 @@ def run_ours(args):
         m_e2e = 0
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        for x in host_steps:
+        for i, x in enumerate(host_steps):
+            if new_turn(n_dev + i):
+                for r in range(w.B):
+                    ctx.extend(r, ext_rows, w.turn_tokens, stream=stream.cuda_stream)
             ctx.assemble_host(req_h, x, slots_h, hits_h, misses_h, stream=stream.cuda_stream)
             if w.appends:
                 ctx.write_back(req, wb_rows, stream=stream.cuda_stream)
@@ -427,6 +454,7 @@ def run_ours(args):
             "config": {"workload": w.name, "batch": w.B, "layers": w.L, "context": w.ctx, "topk": w.k,
                        "hot_slots": w.S, "fresh": w.fresh, "row_bytes": rb, "row_dtype": "bf16",
                        "write_back_per_step": w.appends, "cuda_graph": use_graph,
+                       "layered": layered, "turn_every": w.turn_every, "turn_tokens": w.turn_tokens,
                        "l2": "inputs larger than L2: each step writes the missed rows (~0.6 GB) into a "
                              f"{w.hot_bytes() / 1e9:.2f} GB hot buffer and reads {w.B * w.L * w.max_context * 4 / 1e6:.0f} MB "
                              "of token->slot maps; no flush"},
@@ -451,7 +479,8 @@ def run_ours(args):
             "warmup_steps_ms": [round(t, 3) for t, _ in warm],
             "link_gbs": link,
             "e2e": e2e,
-            "gpu_launches": K * (2 + (2 if w.appends else 0)),
+            "gpu_launches": K * (2 * per_call + (2 if w.appends else 0))
+                            + sum(2 * w.B for s in range(W, n_dev) if new_turn(s)),
             "clocks": clocks,
             "cpu_baseline": cpu,
             "setup": {"pool_gb": w.pool_bytes() / 1e9, "pool_fill_s": fill_s},

@@ -149,6 +149,19 @@ SKV_API skv_status skv_publish(skv_ctx *ctx, const void *rows, int64_t T, int32_
 SKV_API skv_status skv_write_back(skv_ctx *ctx, const int32_t *req_ids_dev, int32_t n, const void *rows_dev,
                           skv_stream_t stream);
 
+/* Extend a request by n tokens at once (the next turn of an agent session:
+ * "XM-Sparse: Netpreme X-Mem ...", section "为何稀疏注意力需要快速高容量内存层" --
+ * coding agents keep hundreds of sessions and reuse up to 95 % of a session's
+ * KV from turn to turn).  rows [L][n][row_bytes] (device memory, or host memory
+ * the device can read, 16-byte aligned) are stored into the pool at positions
+ * [len, len + n) of every layer and len grows by n.  Unlike release + publish,
+ * the request keeps its maps and its hot buffer, so the previous turns' tokens
+ * that are still resident keep hitting.  Host errors: SKV_ERR_BAD_REQUEST (not
+ * an active request), SKV_ERR_CONTEXT_FULL (n > max_context),
+ * SKV_ERR_INVALID_ARG; device error bits: SKV_DEVERR_CONTEXT_FULL when
+ * len + n > max_context (nothing written).  n == 0 enqueues nothing. */
+SKV_API skv_status skv_extend(skv_ctx *ctx, int32_t req, const void *rows, int64_t n, skv_stream_t stream);
+
 /* One decode step (lifecycle step "acquire"): for each batch entry b < B and
  * layer l, make every token of topk_dev[b][l][0..k) resident in the hot
  * buffer of request req_ids_dev[b], layer l, and write its slot index to

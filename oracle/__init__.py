@@ -61,6 +61,8 @@ def load(path: str | None = None):
     L.orc_release.argtypes = [vp, i32]
     L.orc_write_back.restype = i32
     L.orc_write_back.argtypes = [vp, vp, i32, vp]
+    L.orc_extend.restype = i32
+    L.orc_extend.argtypes = [vp, i32, vp, i64]
     L.orc_assemble.restype = i32
     L.orc_assemble.argtypes = [vp, vp, i32, vp, vp, vp, vp, i32]
     L.orc_assemble_layer.restype = i32
@@ -137,6 +139,13 @@ class Oracle:
         rows = np.ascontiguousarray(rows, dtype=np.uint8)
         assert rows.size == req.size * self.L * self.row_bytes
         return int(self.lib.orc_write_back(self.h, _ptr(req), req.size, _ptr(rows)))
+
+    def extend(self, r: int, rows: np.ndarray) -> int:
+        """Append rows [L][n][row_bytes] to request r."""
+        rows = np.ascontiguousarray(rows, dtype=np.uint8)
+        n = rows.size // (self.L * self.row_bytes)
+        assert rows.size == n * self.L * self.row_bytes
+        return int(self.lib.orc_extend(self.h, r, _ptr(rows), n))
 
     def assemble(self, req_ids, topk: np.ndarray, nthreads: int = 1):
         """Returns (err, slots[B][L][k], hits[B][L], misses[B][L])."""

@@ -318,6 +318,29 @@ int32_t orc_assemble_layer(void* h, const int32_t* req_ids, int32_t B, int32_t l
     return assemble_units(o, req_ids, B, layer, topk, slots, hits, misses, nthreads);
 }
 
+// Append n rows per layer to request r: rows is [L][n][row_bytes].  Returns
+// the error bits (0 on success; the sticky word if already set), or -1 if r
+// is not an active request (nothing changes).
+int32_t orc_extend(void* h, int32_t r, const uint8_t* rows, int64_t n)
+{
+    Oracle* o = static_cast<Oracle*>(h);
+    if (r < 0 || r >= o->R || !o->req[r].active) return -1;
+    if (n <= 0) return 0;
+    if (o->err) return o->err;
+    Request& q = o->req[r];
+    if (q.len + n > o->T_max) {
+        o->err |= E_CONTEXT_FULL;
+        return E_CONTEXT_FULL;
+    }
+    for (int32_t l = 0; l < o->L; ++l)
+        for (int64_t j = 0; j < n; ++j) {
+            const uint8_t* src = rows + ((size_t)l * n + j) * o->row_bytes;
+            q.units[l].appended[q.len + j] = std::vector<uint8_t>(src, src + o->row_bytes);
+        }
+    q.len += n;
+    return 0;
+}
+
 // Read and clear the sticky error word.
 int32_t orc_get_error(void* h)
 {

@@ -115,6 +115,8 @@ class Workload:
     lifecycle_step: int = -1        # release + publish of batch entry 1 before this step
     max_requests: int = 0           # 0 -> B
     seed: int = 0
+    turn_every: int = 0             # agent sessions: every turn_every steps each request
+    turn_tokens: int = 0            # grows by turn_tokens tokens (skv_extend)
 
     @property
     def R(self) -> int:
@@ -127,7 +129,15 @@ class Workload:
 
     @property
     def max_context(self) -> int:
-        return self.ctx + (self.steps if self.appends else 0)
+        return self.len_at(self.steps)
+
+    def len_at(self, s: int) -> int:
+        """Context length of every request during step s (before that step's
+        write back, after that step's turn extension)."""
+        n = self.ctx + (s if self.appends else 0)
+        if self.turn_every:
+            n += (s // self.turn_every) * self.turn_tokens
+        return n
 
     @property
     def base_seed(self) -> int:
@@ -160,6 +170,12 @@ WORKLOADS = {
                                    fresh=0.2, lifecycle_step=32),
     "target_16k_b192_f20": Workload("target_16k_b192_f20", B=192, L=8, ctx=16384, k=2048, S=4096, steps=128,
                                     fresh=0.2),
+    # agent sessions: each request is a session whose KV grows by 5 % per turn
+    # (a new turn every 16 decode steps), so ~95 % of its KV is reused; fresh
+    # picks favour the newest turn's tokens
+    "agentic_16k_b64_turns": Workload("agentic_16k_b64_turns", B=64, L=8, ctx=15565, k=2048, S=4096, steps=128,
+                                      fresh=0.2, dist=DIST_RECENCY, window=819, p_window=0.7, turn_every=16,
+                                      turn_tokens=819),
 }
 
 

@@ -74,5 +74,6 @@ cudaError_t prepare_step_kernels(int k, int S, int* gather_grid);
 cudaError_t launch_reset_request(const Dev& d, int r, int64_t len, int active, cudaStream_t st);
 cudaError_t launch_init_lru_all(const Dev& d, cudaStream_t st);
 cudaError_t launch_write_back(const Dev& d, const int32_t* req_ids, int n, const void* rows, cudaStream_t st);
+cudaError_t launch_extend(const Dev& d, int r, int64_t n, const void* rows, cudaStream_t st);
 
 }  // namespace skv

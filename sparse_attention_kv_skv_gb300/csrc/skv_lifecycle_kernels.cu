@@ -78,7 +78,54 @@ __global__ void __launch_bounds__(kLifecycleThreads) write_back_copy_kernel(Dev 
     }
 }
 
+// extend, phase 1 (one thread): the request must be active and its pool region
+// must have room for n more rows; on success reserve [len, len + n).
+__global__ void extend_check_kernel(Dev d, int r, int64_t n)
+{
+    if (threadIdx.x != 0 || d.ctl[CTL_ERR] != 0) return;  // sticky error: no-op
+    uint32_t f = 0;
+    if (d.active[r] == 0) f |= DEVERR_BAD_REQUEST;
+    else if (d.len[r] + n > d.T_max) f |= DEVERR_CONTEXT_FULL;
+    if (f) {
+        d.ctl[CTL_ERR] |= f;
+        return;
+    }
+    d.wb_pos[0] = d.len[r];
+    d.len[r] += n;
+}
+
+// extend, phase 2: rows [L][n][row_bytes] -> pool rows [len, len + n) of each
+// layer of request r, 16-byte chunks through the mapped pool.
+__global__ void __launch_bounds__(kLifecycleThreads) extend_copy_kernel(Dev d, int r, int64_t n,
+                                                                        const int4* __restrict__ rows)
+{
+    if (d.ctl[CTL_ERR] != 0) return;
+    const int cpr = d.row_bytes / 16;
+    const int64_t total = (int64_t)d.L * n * cpr;
+    const int64_t pos = d.wb_pos[0];
+    int4* pool = reinterpret_cast<int4*>(d.pool);
+    for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < total; c += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t rowi = c / cpr;  // = l*n + j
+        const int w = (int)(c - rowi * cpr);
+        const int l = (int)(rowi / n);
+        const int64_t j = rowi - (int64_t)l * n;
+        pool[(((int64_t)r * d.L + l) * d.T_max + pos + j) * cpr + w] = rows[c];
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_extend(const Dev& d, int r, int64_t n, const void* rows, cudaStream_t st)
+{
+    extend_check_kernel<<<1, 32, 0, st>>>(d, r, n);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int64_t total = (int64_t)d.L * n * (d.row_bytes / 16);
+    int64_t g = (total + kLifecycleThreads - 1) / kLifecycleThreads;
+    const int grid = (int)(g < 4096 ? g : 4096);
+    extend_copy_kernel<<<grid, kLifecycleThreads, 0, st>>>(d, r, n, reinterpret_cast<const int4*>(rows));
+    return cudaGetLastError();
+}
 
 cudaError_t launch_reset_request(const Dev& d, int r, int64_t len, int active, cudaStream_t st)
 {

@@ -324,6 +324,18 @@ skv_status assemble_impl(skv_ctx* ctx, const Dev& d, const int32_t* req_ids_dev,
 
 extern "C" {
 
+skv_status skv_extend(skv_ctx* ctx, int32_t req, const void* rows, int64_t n, skv_stream_t stream)
+{
+    if (!ctx || n < 0) return SKV_ERR_INVALID_ARG;
+    if (req < 0 || req >= ctx->cfg.max_requests || !ctx->active_h[req]) return SKV_ERR_BAD_REQUEST;
+    if (n == 0) return SKV_OK;
+    if (!rows || (reinterpret_cast<uintptr_t>(rows) & 15u)) return SKV_ERR_INVALID_ARG;
+    if (n > ctx->cfg.max_context) return SKV_ERR_CONTEXT_FULL;
+    DeviceGuard g(ctx->cfg.device);
+    SKV_CUDA(skv::launch_extend(ctx->d, req, n, rows, stream));
+    return SKV_OK;
+}
+
 skv_status skv_assemble(skv_ctx* ctx, const int32_t* req_ids_dev, int32_t B, const int32_t* topk_dev,
                         int32_t* slots_dev, int32_t* hits_dev, int32_t* misses_dev, skv_stream_t stream)
 {

@@ -57,6 +57,7 @@ def _load():
         "skv_destroy": [vp],
         "skv_publish": [vp, vp, i64, P(i32), vp],
         "skv_write_back": [vp, vp, i32, vp, vp],
+        "skv_extend": [vp, i32, vp, i64, vp],
         "skv_assemble": [vp, vp, i32, vp, vp, vp, vp, vp],
         "skv_assemble_host": [vp, vp, i32, vp, vp, vp, vp, vp],
         "skv_assemble_noalloc": [vp, vp, i32, vp, vp, vp, vp, vp],
@@ -89,6 +90,7 @@ skv_create = lib.skv_create
 skv_destroy = lib.skv_destroy
 skv_publish = lib.skv_publish
 skv_write_back = lib.skv_write_back
+skv_extend = lib.skv_extend
 skv_assemble = lib.skv_assemble
 skv_assemble_host = lib.skv_assemble_host
 skv_assemble_noalloc = lib.skv_assemble_noalloc
@@ -196,6 +198,10 @@ class Context:
     def write_back(self, req_ids, rows, n: int | None = None, stream=None) -> None:
         n = req_ids.numel() if n is None else n
         check(skv_write_back(self.h, _ptr(req_ids), n, _ptr(rows), _stream_handle(stream)), "skv_write_back")
+
+    def extend(self, req: int, rows, n: int, stream=None) -> None:
+        """Append n tokens' rows [L][n][row_bytes] to request req."""
+        check(skv_extend(self.h, req, _ptr(rows), n, _stream_handle(stream)), "skv_extend")
 
     def assemble(self, req_ids, topk, slots, hits, misses, B: int | None = None, stream=None) -> None:
         B = req_ids.numel() if B is None else B

@@ -464,3 +464,45 @@ def check_layer_mode(lib_path=None, steps=6):
     full.close()
     per.close()
     gen.close()
+
+
+# ----------------------------------------------------------------------------
+# extend = n write backs
+# ----------------------------------------------------------------------------
+
+def check_extend(lib_path=None):
+    """Extending a request by n rows leaves the pool and the request exactly as
+    n single-row write backs do; a full region rejects the whole extension."""
+    R, L, T, k, S = 2, 2, 10, 3, 4
+    T_max = 16
+    pool = make_pool(R, L, T_max, seed=31, T=T)
+    a = orc.Oracle(R, L, T_max, RB, k, S, pool, lib_path=lib_path)
+    b = orc.Oracle(R, L, T_max, RB, k, S, pool, lib_path=lib_path)
+    for o in (a, b):
+        assert o.publish(T) == 0 and o.publish(T) == 1
+        assert o.assemble([0, 1], np.array([[[1, 2, 3], [4, 5, 6]], [[7, 8, 9], [0, 1, 2]]], np.int32))[0] == 0
+    n = 4
+    rows = np.stack([wl.fill_rows(77, 1, l, T, n, ROW_ELEMS) for l in range(L)])   # [L][n][RB]
+    assert a.extend(1, rows) == 0
+    for j in range(n):
+        assert b.write_back([1], rows[:, j, :][None]) == 0
+    for o in (a, b):
+        assert o.export(1)["len"] == T + n and o.export(0)["len"] == T
+    for l in range(L):
+        for j in range(n):
+            assert np.array_equal(a.pool_row(1, l, T + j), rows[l, j])
+            assert np.array_equal(b.pool_row(1, l, T + j), rows[l, j])
+    for r in range(R):
+        ea, eb = a.export(r), b.export(r)
+        for key in ("slot2tok", "ts", "lru", "tok2slot"):
+            assert np.array_equal(ea[key], eb[key]), key
+    # the new tokens are selectable, and miss on first use
+    e, slots, hits, misses = a.assemble([1], np.array([[[T, T + 3, 1], [T + 1, 0, 2]]], np.int32))
+    assert e == 0 and misses.tolist() == [[3, 1]]   # layer 0 holds {7, 8, 9}; layer 1 holds {0, 1, 2}
+    # a region without room for all n rows is rejected whole
+    big = np.zeros((L, T_max - (T + n) + 1, RB), np.uint8)
+    assert a.extend(1, big) == orc.E_CONTEXT_FULL
+    assert a.export(1)["len"] == T + n and a.get_error() == orc.E_CONTEXT_FULL
+    assert a.extend(5, rows) == -1 and a.extend(1, rows[:, :0]) == 0
+    a.close()
+    b.close()

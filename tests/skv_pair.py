@@ -100,8 +100,29 @@ class Pair:
         torch.cuda.current_stream().wait_stream(side)
         torch.cuda.synchronize()
 
-    def step(self, s: int, compare: bool = True):
+    def extend_all(self, n: int, republish: bool = False) -> None:
+        """A new turn for every session: n more tokens per request (skv_extend),
+        or -- the cold alternative -- release and publish the grown request."""
         w = self.w
+        for b, r in enumerate(self.req_ids):
+            key = w.req_key(r, self.generation[r])
+            if republish:
+                self.ctx.release(r)
+                assert self.orc.release(r) == 0
+                new_len = self.lens[b] + n
+                assert self.ctx.publish(new_len) == r and self.orc.publish(new_len) == r
+                torch.cuda.synchronize()
+                wl.fill_request(self.req_base(r), w.L, self.T_max, new_len, w.base_seed, key)
+            else:
+                rows = np.stack([wl.fill_rows(w.base_seed, key, l, self.lens[b], n) for l in range(w.L)])
+                self.ctx.extend(r, torch.from_numpy(rows).to(self.dev), n)
+                assert self.orc.extend(r, rows) == 0
+            self.lens[b] += n
+
+    def step(self, s: int, compare: bool = True, republish: bool = False):
+        w = self.w
+        if w.turn_every and s > 0 and s % w.turn_every == 0:
+            self.extend_all(w.turn_tokens, republish=republish)
         topk = self.gen.step(s, self.lens)
         self.topk_dev.copy_(torch.from_numpy(topk))
         if getattr(self, "graph", None) is not None:
@@ -180,8 +201,8 @@ class Pair:
 
     def compare_hot_rows(self, reqs) -> None:
         """For the given requests, every resident device row equals its
-        token's pool row (published rows recomputed from the generator,
-        appended rows as written back), and every empty slot is zero."""
+        token's row as the generator defines it, and every empty slot is
+        zero."""
         w = self.w
         for r in reqs:
             st = self.orc.export(r, tok2slot=False)
@@ -192,12 +213,11 @@ class Pair:
                 occ = np.flatnonzero(s2t >= 0)
                 assert not gh[l][s2t < 0].any(), (r, l)
                 toks = s2t[occ]
-                pub = toks < w.ctx
+                # published, extended and written-back rows all follow the
+                # generator's formula for (request key, layer, token)
                 want = np.empty((occ.size, RB), dtype=np.uint8)
-                for j in np.flatnonzero(pub):
+                for j in range(occ.size):
                     want[j] = wl.fill_rows(w.base_seed, key, l, int(toks[j]), 1)[0]
-                for j in np.flatnonzero(~pub):
-                    want[j] = self.appended[(r, l, int(toks[j]))]
                 if not np.array_equal(gh[l][occ], want):
                     bad = np.flatnonzero((gh[l][occ] != want).any(axis=1))
                     raise AssertionError(f"request {r} layer {l}: slot {occ[bad[0]]} (token {toks[bad[0]]}) "

@@ -56,6 +56,8 @@ MUTANTS = {
     "layer_call_not_validated": [
         ("for (int64_t j = 0; j < nl; ++j) {\n            std::unordered_set<int32_t> row_tokens;",
          "for (int64_t j = 0; j < (layer < 0 ? nl : 0); ++j) {\n            std::unordered_set<int32_t> row_tokens;")],
+    "extend_off_by_one": [
+        ("q.units[l].appended[q.len + j] =", "q.units[l].appended[q.len + j + 1] =")],
     "sticky_error_ignored": [
         ("    if (o->err) {\n        reject();\n        return o->err;\n    }", "")],
 }
@@ -83,6 +85,7 @@ checks = [
     lambda: pins.check_invariants(wl.Workload("mut_inv", B=2, L=1, ctx=100, k=12, S=20, steps=6, fresh=0.4,
                                               order=wl.ORDER_SHUFFLED), lib),
     lambda: pins.check_layer_mode(lib, steps=3),
+    lambda: pins.check_extend(lib),
 ]
 for c in checks:
     try:

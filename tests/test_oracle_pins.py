@@ -48,3 +48,7 @@ def test_errors_and_lifecycle():
 
 def test_layer_calls_match_full_steps():
     pins.check_layer_mode()
+
+
+def test_extend_equals_repeated_write_back():
+    pins.check_extend()
