@@ -279,6 +279,20 @@ SKV_API skv_status skv_get_stats(skv_ctx *ctx, uint64_t *calls, uint64_t *hits, 
  * SKV_ERR_INVALID_ARG.  The events belong to the caller. */
 SKV_API skv_status skv_set_gather_events(skv_ctx *ctx, skv_event_t before, skv_event_t after);
 
+/* Diagnostic: one 128 x n x k bf16 matrix product on the tensor cores through
+ * the same path the attention consumer uses (operands staged in shared memory,
+ * tcgen05 MMA into tensor memory, read back by the issuing warpgroup):
+ * d_dev[128][n] (fp32) = a_dev[128][k] * B^T with B = b_dev as [n][k]
+ * row-major (b_mn_major = 0: staged K-major) or B^T = b_dev as [k][n]
+ * row-major (b_mn_major = 1: staged MN-major, the form in which the
+ * attention consumer reads V); device memory, a / b 16-byte aligned,
+ * 16 <= n <= 256 and 16 <= k <= 128, both multiples of 16.  Allocates a
+ * 4-byte status word with cudaMallocAsync and synchronises `stream`.
+ * SKV_ERR_CUDA (with a message) if the MMA does not complete within a bounded
+ * wait.  Not part of any decode step. */
+SKV_API skv_status skv_selftest_mma(const void *a_dev, const void *b_dev, float *d_dev, int32_t n, int32_t k,
+                                    int32_t b_mn_major, skv_stream_t stream);
+
 /* The message of the last failing CUDA call on this thread ("" if none). */
 SKV_API const char *skv_last_cuda_error(void);
 

@@ -20,7 +20,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libskv.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["skv_runtime.cu", "skv_step_kernels.cu", "skv_lifecycle_kernels.cu", "skv_noalloc.cu"]
+SOURCES = ["skv_runtime.cu", "skv_step_kernels.cu", "skv_lifecycle_kernels.cu", "skv_noalloc.cu",
+           "skv_attention.cu"]
 
 
 def nvcc() -> str:

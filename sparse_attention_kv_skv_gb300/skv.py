@@ -71,6 +71,7 @@ def _load():
         "skv_get_clock": [vp, P(ctypes.c_uint32), vp],
         "skv_get_stats": [vp, P(ctypes.c_uint64), P(ctypes.c_uint64), P(ctypes.c_uint64), vp],
         "skv_set_gather_events": [vp, vp, vp],
+        "skv_selftest_mma": [vp, vp, vp, i32, i32, i32, vp],
     }
     for name, args in sigs.items():
         f = getattr(lib, name)
@@ -104,6 +105,7 @@ skv_export_hot = lib.skv_export_hot
 skv_get_clock = lib.skv_get_clock
 skv_get_stats = lib.skv_get_stats
 skv_set_gather_events = lib.skv_set_gather_events
+skv_selftest_mma = lib.skv_selftest_mma
 skv_last_cuda_error = lib.skv_last_cuda_error
 skv_status_string = lib.skv_status_string
 
