@@ -46,6 +46,11 @@ def parse():
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of per-step CUDA graphs")
     ap.add_argument("--layered", action="store_true",
                     help="each step assembles layer by layer (L skv_assemble_layer calls) instead of one call")
+    ap.add_argument("--attend", action="store_true",
+                    help="each step also runs the tensor-core sparse attention (skv_attend) over the assembled slots")
+    ap.add_argument("--pipeline", action="store_true",
+                    help="with --attend: layer by layer, attention of layer l on a second stream overlapping the "
+                         "assembly of layer l+1")
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--cpu-sample-requests", type=int, default=32)
     ap.add_argument("--cpu-sample-steps", type=int, default=24)
@@ -323,6 +328,28 @@ def run_ours(args):
     hits = torch.empty((n_dev, w.L, w.B) if layered else (n_dev, w.B, w.L), dtype=torch.int32, device=dev)
     misses = torch.empty_like(hits)
     stream = torch.cuda.Stream(device=dev)
+    attn_on = args.attend or args.pipeline
+    if args.pipeline and not layered:
+        raise SystemExit("--pipeline needs --layered")
+    if attn_on:
+        # synthetic decode queries (128 heads x 576) per unit, fixed across steps
+        units = [(b, l) for l in range(w.L) for b in range(w.B)] if layered else \
+                [(b, l) for b in range(w.B) for l in range(w.L)]
+        q_host = np.stack([wl.fill_q(w.base_seed, b, l) for b, l in units])
+        q_all = torch.from_numpy(q_host).to(dev).view(torch.int16)
+        q_all = q_all.view(w.L, w.B, 128, 576) if layered else q_all.view(w.B * w.L, 128, 576)
+        att_out = torch.empty((w.L, w.B, 128, 512) if layered else (w.B * w.L, 128, 512), dtype=torch.int16,
+                              device=dev)
+        att_lse = torch.empty((w.L, w.B, 128) if layered else (w.B * w.L, 128), dtype=torch.float32, device=dev)
+        side = torch.cuda.Stream(device=dev)
+        ev_layer = [torch.cuda.Event() for _ in range(w.L)]
+        ev_join = torch.cuda.Event()
+        del q_host
+        # serial mode: time every step's attention call
+        att_b = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n_dev)]
+        att_a = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n_dev)]
+        for ev in att_b + att_a:
+            ev.record(stream)
     n_ev = n_dev * (w.L if layered else 1)  # one pair per assemble call
     ev_b = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n_ev)]
     ev_a = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n_ev)]
@@ -341,9 +368,22 @@ def run_ours(args):
                 ctx.set_gather_events(ev_b[e], ev_a[e])
                 ctx.assemble_layer(l, req, topk_all[s, l], slots[l], hits[s, l], misses[s, l],
                                    stream=stream.cuda_stream)
+                if attn_on:
+                    astream = side if args.pipeline else stream
+                    if args.pipeline:
+                        ev_layer[l].record(stream)
+                        side.wait_event(ev_layer[l])
+                    ctx.attend(req, q_all[l], slots[l], att_out[l], att_lse[l], layer=l, stream=astream.cuda_stream)
+            if args.pipeline:
+                ev_join.record(side)
+                stream.wait_event(ev_join)
         else:
             ctx.set_gather_events(ev_b[s], ev_a[s])
             ctx.assemble(req, topk_all[s], slots, hits[s], misses[s], stream=stream.cuda_stream)
+            if attn_on:
+                att_b[s].record(stream)
+                ctx.attend(req, q_all, slots, att_out, att_lse, stream=stream.cuda_stream)
+                att_a[s].record(stream)
         if w.appends:
             ctx.write_back(req, wb_rows, stream=stream.cuda_stream)
 
@@ -403,6 +443,23 @@ def run_ours(args):
     for m_s, h_s in zip(per_step_m, per_step_h):
         t_roof += max(m_s * rb / (link["h2d"] * 1e9), hbm_algorithmic_bytes(w, int(m_s), int(h_s)) / (hbm_peak * 1e9))
 
+    attention = None
+    if attn_on:
+        flops = float(2 * 128 * (576 + 512)) * tokens  # per valid Top-k entry: q.k over 576, p.v over 512, 128 heads
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+            os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+        tpeak = float(peaks.get("bf16_tflops_sustained", 1700.0))
+        attention = {"heads": 128, "dims": 576, "value_dims": 512, "algorithmic_flops_per_step": flops / K,
+                     "tensor_peak_tflops": tpeak,
+                     "tensor_peak_source": "MEASURED_PEAKS.json bf16_tflops_sustained (kernel timed inside a step)"
+                     if "bf16_tflops_sustained" in peaks else "fallback 1.7 PFLOP/s sustained"}
+        if not layered:
+            att_s = sum(event_ms(att_b[s], att_a[s]) for s in range(W, n_dev)) / 1e3
+            attention.update({"kernel": "attend_kernel (tcgen05)", "ms_per_step": 1e3 * att_s / K,
+                              "tflops": flops / att_s / 1e12, "frac_of_tensor_peak": flops / att_s / 1e12 / tpeak,
+                              "key_bytes_per_step": tokens * rb / K,
+                              "key_gbs": tokens * rb / att_s / 1e9})
+
     # end to end through the host-buffer entry point
     e2e = None
     if args.e2e_steps > 0:
@@ -455,6 +512,7 @@ def run_ours(args):
                        "hot_slots": w.S, "fresh": w.fresh, "row_bytes": rb, "row_dtype": "bf16",
                        "write_back_per_step": w.appends, "cuda_graph": use_graph,
                        "layered": layered, "turn_every": w.turn_every, "turn_tokens": w.turn_tokens,
+                       "attend": attn_on, "pipeline": bool(args.pipeline),
                        "l2": "inputs larger than L2: each step writes the missed rows (~0.6 GB) into a "
                              f"{w.hot_bytes() / 1e9:.2f} GB hot buffer and reads {w.B * w.L * w.max_context * 4 / 1e6:.0f} MB "
                              "of token->slot maps; no flush"},
@@ -477,9 +535,10 @@ def run_ours(args):
             "cold_step": {"ms": warm[0][0], "missed_rows": warm[0][1],
                           "gbs": warm[0][1] * rb / warm[0][0] / 1e6} if rank == 0 else None,
             "warmup_steps_ms": [round(t, 3) for t, _ in warm],
+            "attention": attention,
             "link_gbs": link,
             "e2e": e2e,
-            "gpu_launches": K * (2 * per_call + (2 if w.appends else 0))
+            "gpu_launches": K * (2 * per_call + (per_call if attn_on else 0) + (2 if w.appends else 0))
                             + sum(2 * w.B for s in range(W, n_dev) if new_turn(s)),
             "clocks": clocks,
             "cpu_baseline": cpu,

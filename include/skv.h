@@ -101,7 +101,8 @@ typedef enum {
 #define SKV_DEVERR_BAD_REQUEST 1   /* a request id in [0,R) that is not active, out of range, or repeated in one call */
 #define SKV_DEVERR_BAD_INDEX 2     /* a Top-k entry that is neither -1 nor in [0, len of its request) */
 #define SKV_DEVERR_DUPLICATE 4     /* a token that appears twice in one (request, layer) Top-k row */
-#define SKV_DEVERR_CONTEXT_FULL 8  /* skv_write_back on a request whose pool region holds max_context tokens */
+#define SKV_DEVERR_CONTEXT_FULL 8  /* skv_write_back / skv_extend beyond max_context tokens */
+#define SKV_DEVERR_TIMEOUT 16      /* skv_attend: a tensor-core product did not complete within its bounded wait */
 
 typedef struct {
     int32_t max_requests;  /* R >= 1: request slots */
@@ -237,6 +238,30 @@ SKV_API skv_status skv_assemble_noalloc(skv_ctx *ctx, const int32_t *req_ids_dev
  * skv_publish may hand the same id out again.  SKV_ERR_BAD_REQUEST if req is
  * not an active request. */
 SKV_API skv_status skv_release(skv_ctx *ctx, int32_t req, skv_stream_t stream);
+
+/* Sparse MLA decode attention over assembled slots (the "compute" of
+ * select-then-compute: "SGLang и Tair представили иерархичную Sparse Attention
+ * ...", paragraph 2; the consumer of the slot tensor the index-copy step emits,
+ * "Sparse Attention-Driven KVCache Management for Domestic AI Supernodes",
+ * agenda item 2).  For each unit (batch entry b, layer l) of the call -- all L
+ * layers when layer == -1 (units ordered b*L + l), else only `layer` (units
+ * ordered b) -- with r = req_ids_dev[b]:
+ *   keys_j = hot row (r, l, slots[unit][j]) for j < k, masked where the slot
+ *            is -1 (or outside [0, S));
+ *   s_hj   = sm_scale * sum_{d<576} q[unit][h][d] * keys_j[d]   (h < 128 heads)
+ *   out[unit][h][0..512) = sum_j softmax_j(s_h)_j * keys_j[0..512)
+ *   lse[unit][h] = log sum_j exp(s_hj)   (-inf and zero output if all masked)
+ * q_dev is [units][128][576] bf16, slots_dev [units][k] int32 (as emitted by
+ * skv_assemble / skv_assemble_layer), out_dev [units][128][512] bf16, lse_dev
+ * [units][128] fp32 (may be null); device memory, q / out 16-byte aligned.
+ * Requires row_bytes == 1152 (576 bf16).  Runs on the tensor cores (tcgen05):
+ * QK^T and PV in tensor memory, fp32 accumulation, P rounded to bf16.
+ * Reads the hot buffer, so order it after the assemble that filled the slots
+ * and before the next assemble of the same layer.  A product that does not
+ * complete within a bounded wait sets SKV_DEVERR_TIMEOUT. */
+SKV_API skv_status skv_attend(skv_ctx *ctx, const int32_t *req_ids_dev, int32_t B, int32_t layer, const void *q_dev,
+                              const int32_t *slots_dev, void *out_dev, float *lse_dev, float sm_scale,
+                              skv_stream_t stream);
 
 /* Read the sticky device error word into *bits (SKV_DEVERR_* mask, 0 = none)
  * and clear it.  Synchronises `stream`. */

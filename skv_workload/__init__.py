@@ -187,6 +187,15 @@ def fill_rows(seed: int, req_key: int, layer: int, t0: int, n: int, row_elems: i
     return out
 
 
+Q_HEADS = 128
+
+
+def fill_q(seed: int, b: int, layer: int, heads: int = Q_HEADS, row_elems: int = ROW_ELEMS) -> np.ndarray:
+    """Synthetic decode queries of batch entry b, layer `layer`: [heads][row_elems]
+    bf16 (as bytes), uniform in [-1, 1), from their own SplitMix64 streams."""
+    return fill_rows(seed ^ 0x5155455259, 0x51 << 48 | b, layer, 0, heads, row_elems)
+
+
 def fill_rows_into(ptr: int, stride: int, seed: int, req_key: int, layer: int, t0: int, n: int,
                    row_elems: int = ROW_ELEMS) -> None:
     lib().skvw_fill_rows(ptr, stride, seed, req_key, layer, t0, n, row_elems)

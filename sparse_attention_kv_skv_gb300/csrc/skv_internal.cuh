@@ -25,7 +25,13 @@ enum : int {
 };
 enum : int { STAT_CALLS = 0, STAT_HITS = 1, STAT_MISSES = 2, STAT_WORDS = 3 };
 
-enum : uint32_t { DEVERR_BAD_REQUEST = 1, DEVERR_BAD_INDEX = 2, DEVERR_DUPLICATE = 4, DEVERR_CONTEXT_FULL = 8 };
+enum : uint32_t {
+    DEVERR_BAD_REQUEST = 1,
+    DEVERR_BAD_INDEX = 2,
+    DEVERR_DUPLICATE = 4,
+    DEVERR_CONTEXT_FULL = 8,
+    DEVERR_TIMEOUT = 16  // a tensor-core product did not signal completion within its bounded wait
+};
 
 // Everything a kernel needs to find the state of unit u = r*L + l.
 struct Dev {
@@ -69,6 +75,11 @@ cudaError_t launch_plan_gather(const Dev& d, const int32_t* req_ids, int B, cons
 // CTAs of the fused kernel that fit on the device at once for (k, S).
 int plan_resident_ctas(int k, int S);
 cudaError_t prepare_step_kernels(int k, int S, int* gather_grid);
+
+// Attention over assembled slots (tensor cores).
+size_t attend_smem_bytes();
+cudaError_t launch_attend(const Dev& d, const int32_t* req_ids, int B, const void* q, const int32_t* slots,
+                          void* out, float* lse, float sm_scale, cudaStream_t st);
 
 // Lifecycle kernels.
 cudaError_t launch_reset_request(const Dev& d, int r, int64_t len, int active, cudaStream_t st);

@@ -30,6 +30,7 @@ SKV_DEVERR_BAD_REQUEST = 1
 SKV_DEVERR_BAD_INDEX = 2
 SKV_DEVERR_DUPLICATE = 4
 SKV_DEVERR_CONTEXT_FULL = 8
+SKV_DEVERR_TIMEOUT = 16
 
 
 class skv_config(ctypes.Structure):
@@ -72,6 +73,7 @@ def _load():
         "skv_get_stats": [vp, P(ctypes.c_uint64), P(ctypes.c_uint64), P(ctypes.c_uint64), vp],
         "skv_set_gather_events": [vp, vp, vp],
         "skv_selftest_mma": [vp, vp, vp, i32, i32, i32, vp],
+        "skv_attend": [vp, vp, i32, i32, vp, vp, vp, vp, ctypes.c_float, vp],
     }
     for name, args in sigs.items():
         f = getattr(lib, name)
@@ -106,6 +108,7 @@ skv_get_clock = lib.skv_get_clock
 skv_get_stats = lib.skv_get_stats
 skv_set_gather_events = lib.skv_set_gather_events
 skv_selftest_mma = lib.skv_selftest_mma
+skv_attend = lib.skv_attend
 skv_last_cuda_error = lib.skv_last_cuda_error
 skv_status_string = lib.skv_status_string
 
@@ -228,6 +231,15 @@ class Context:
         B = len(req_ids) if B is None else B
         check(skv_assemble_host(self.h, _ptr(req_ids), B, _ptr(topk), _ptr(slots), _ptr(hits), _ptr(misses),
                                 _stream_handle(stream)), "skv_assemble_host")
+
+    def attend(self, req_ids, q, slots, out, lse=None, layer: int = -1, sm_scale: float | None = None,
+               B: int | None = None, stream=None) -> None:
+        """Sparse MLA attention over assembled slots (see skv_attend):
+        q [units][128][576] bf16 -> out [units][128][512] bf16, lse [units][128]."""
+        B = req_ids.numel() if B is None else B
+        scale = (1.0 / 576 ** 0.5) if sm_scale is None else sm_scale
+        check(skv_attend(self.h, _ptr(req_ids), B, layer, _ptr(q), _ptr(slots), _ptr(out), _ptr(lse), scale,
+                         _stream_handle(stream)), "skv_attend")
 
     # inspection ------------------------------------------------------------
     def get_device_error(self, stream=None) -> int:

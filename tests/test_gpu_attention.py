@@ -1,0 +1,97 @@
+"""skv_attend (tensor-core sparse MLA attention over assembled slots) against
+the fp64 attention oracle evaluated on the CPU oracle's own hot buffer (GPU).
+
+Tolerance, from the arithmetic: q and the key rows are bf16, their products
+are exact in fp32 and summed in fp32 (|error of s| << 1e-3 at these scales);
+the probabilities P enter the second product rounded to bf16 (relative error
+<= 2^-9), so |error of out| <= 2^-9 * max|V| = 2e-3 with |V| <= 1; the output
+is rounded to bf16 (another 2^-9 |out|).  The test allows 6e-3 + 6e-3 |out|
+(x3 margin) and 5e-3 on lse.
+"""
+import numpy as np
+import pytest
+import torch
+
+import skv_workload as wl
+from oracle import attention as att
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    from skv_pair import Pair
+
+ATOL, RTOL, LSE_ATOL = 6e-3, 6e-3, 5e-3
+
+
+def _queries(w, units):
+    """[units][128][576] bf16 for the given (b, l) list."""
+    return np.stack([wl.fill_q(w.base_seed, b, l) for b, l in units]).view(np.uint16)
+
+
+def _check_units(p, units, slots, q, out, lse, scale):
+    hot_cache = {}
+    for n, (b, l) in enumerate(units):
+        r = p.req_ids[b]
+        if r not in hot_cache:
+            hot_cache[r] = p.orc.export_hot(r)
+        row = slots[n]
+        valid = row >= 0
+        keys = np.zeros((row.size, 576))
+        keys[valid] = att.bf16_rows_to_f64(hot_cache[r][l][row[valid]])
+        want, want_lse = att.attend(att.bf16_rows_to_f64(q[n].view(np.uint8)), keys, valid, scale)
+        got = att.bf16_rows_to_f64(out[n].view(np.uint8))
+        err = np.abs(got - want) - (ATOL + RTOL * np.abs(want))
+        assert err.max() <= 0, f"unit {(b, l)}: out off by {np.abs(got - want).max()}"
+        both_inf = np.isneginf(want_lse) & np.isneginf(lse[n])
+        diff = np.abs(np.where(both_inf, 0.0, lse[n] - want_lse))
+        assert np.all(diff <= LSE_ATOL), f"unit {(b, l)}: lse"
+
+
+@pytest.mark.parametrize("scale", [1.0 / 24.0, 0.35])
+def test_attention_over_assembled_slots(scale):
+    w = wl.Workload("attn", B=3, L=2, ctx=3000, k=300, S=512, steps=3, fresh=0.3, order=wl.ORDER_SHUFFLED,
+                    n_pad=7)
+    p = Pair(w, req_perm=[2, 0, 1])
+    try:
+        for s in range(w.steps):
+            p.step(s)
+        units = [(b, l) for b in range(w.B) for l in range(w.L)]
+        q = _queries(w, units)
+        q_d = torch.from_numpy(q).cuda()
+        out_d = torch.full((len(units), 128, 512), 0x7FC0, dtype=torch.int16, device="cuda")
+        lse_d = torch.full((len(units), 128), float("nan"), device="cuda")
+        p.ctx.attend(p.req_dev, q_d, p.slots_dev, out_d, lse_d, sm_scale=scale)
+        slots = p.slots_dev.cpu().numpy().reshape(len(units), w.k)
+        _check_units(p, units, slots, q, out_d.cpu().numpy().view(np.uint16), lse_d.cpu().numpy(), scale)
+        assert p.ctx.get_device_error() == 0
+    finally:
+        p.close()
+
+
+def test_attention_one_layer_and_fully_masked_units():
+    w = wl.Workload("attn1", B=4, L=3, ctx=2500, k=256, S=400, steps=2, fresh=0.3)
+    p = Pair(w)
+    try:
+        for s in range(w.steps):
+            p.step(s)
+        layer = 1
+        # one batch entry selects nothing in this layer: all -1
+        topk = p.gen.step(w.steps, p.lens)[:, layer, :].copy()
+        topk[2, :] = -1
+        t_d = torch.from_numpy(topk).cuda()
+        slots_d = torch.empty_like(t_d)
+        hm = torch.empty(w.B, dtype=torch.int32, device="cuda")
+        p.ctx.assemble_layer(layer, p.req_dev, t_d, slots_d, hm, hm.clone())
+        e, o_slots, _, _ = p.orc.assemble_layer(layer, p.req_ids, topk)
+        assert e == 0 and np.array_equal(slots_d.cpu().numpy(), o_slots)
+        units = [(b, layer) for b in range(w.B)]
+        q = _queries(w, units)
+        out_d = torch.empty((w.B, 128, 512), dtype=torch.int16, device="cuda")
+        lse_d = torch.empty((w.B, 128), device="cuda")
+        p.ctx.attend(p.req_dev, torch.from_numpy(q).cuda(), slots_d, out_d, lse_d, layer=layer, sm_scale=0.2)
+        out = out_d.cpu().numpy().view(np.uint16)
+        lse = lse_d.cpu().numpy()
+        _check_units(p, units, o_slots, q, out, lse, 0.2)
+        assert not out[2].any() and np.all(np.isneginf(lse[2]))
+    finally:
+        p.close()
