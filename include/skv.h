@@ -253,9 +253,13 @@ SKV_API skv_status skv_release(skv_ctx *ctx, int32_t req, skv_stream_t stream);
  *   lse[unit][h] = log sum_j exp(s_hj)   (-inf and zero output if all masked)
  * q_dev is [units][128][576] bf16, slots_dev [units][k] int32 (as emitted by
  * skv_assemble / skv_assemble_layer), out_dev [units][128][512] bf16, lse_dev
- * [units][128] fp32 (may be null); device memory, q / out 16-byte aligned.
+ * [units][128] fp32 (may be null); device memory, q / out 16-byte aligned;
+ * sm_scale finite and > 0 (else SKV_ERR_INVALID_ARG).
  * Requires row_bytes == 1152 (576 bf16).  Runs on the tensor cores (tcgen05):
- * QK^T and PV in tensor memory, fp32 accumulation, P rounded to bf16.
+ * QK^T and PV in tensor memory, fp32 accumulation, P rounded to bf16; a
+ * cluster of two CTAs per unit, each owning half of the score dims and half of
+ * the value dims, with the partial scores summed through distributed shared
+ * memory.
  * Reads the hot buffer, so order it after the assemble that filled the slots
  * and before the next assemble of the same layer.  A product that does not
  * complete within a bounded wait sets SKV_DEVERR_TIMEOUT. */
@@ -305,18 +309,21 @@ SKV_API skv_status skv_get_stats(skv_ctx *ctx, uint64_t *calls, uint64_t *hits, 
 SKV_API skv_status skv_set_gather_events(skv_ctx *ctx, skv_event_t before, skv_event_t after);
 
 /* Diagnostic: one 128 x n x k bf16 matrix product on the tensor cores through
- * the same path the attention consumer uses (operands staged in shared memory,
- * tcgen05 MMA into tensor memory, read back by the issuing warpgroup):
- * d_dev[128][n] (fp32) = a_dev[128][k] * B^T with B = b_dev as [n][k]
- * row-major (b_mn_major = 0: staged K-major) or B^T = b_dev as [k][n]
- * row-major (b_mn_major = 1: staged MN-major, the form in which the
- * attention consumer reads V); device memory, a / b 16-byte aligned,
- * 16 <= n <= 256 and 16 <= k <= 128, both multiples of 16.  Allocates a
- * 4-byte status word with cudaMallocAsync and synchronises `stream`.
- * SKV_ERR_CUDA (with a message) if the MMA does not complete within a bounded
- * wait.  Not part of any decode step. */
+ * the same path the attention consumer uses (tcgen05 MMA into tensor memory,
+ * read back by the issuing warpgroup):
+ * d_dev[128][n] (fp32) = a_dev[128][k] * B^T.  `mode` bit 0 clear: B = b_dev
+ * as [n][k] row-major, staged K-major; set: B^T = b_dev as [k][n] row-major,
+ * staged MN-major (the form in which the attention consumer reads V).  Bit 1
+ * clear: A staged K-major in shared memory; set: A written to tensor memory
+ * (row m in lane m, two bf16 per 32-bit column) and read from there (the form
+ * in which the attention consumer holds Q).  Device memory, a / b 16-byte
+ * aligned, 16 <= n <= 256 and 16 <= k <= 128, both multiples of 16,
+ * 0 <= mode <= 3, else SKV_ERR_INVALID_ARG.  Allocates a 4-byte status word
+ * with cudaMallocAsync and synchronises `stream`.  SKV_ERR_CUDA (with a
+ * message) if the MMA does not complete within a bounded wait.  Not part of
+ * any decode step. */
 SKV_API skv_status skv_selftest_mma(const void *a_dev, const void *b_dev, float *d_dev, int32_t n, int32_t k,
-                                    int32_t b_mn_major, skv_stream_t stream);
+                                    int32_t mode, skv_stream_t stream);
 
 /* The message of the last failing CUDA call on this thread ("" if none). */
 SKV_API const char *skv_last_cuda_error(void);

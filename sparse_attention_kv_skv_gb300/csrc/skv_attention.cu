@@ -10,17 +10,33 @@
 // 576 dims; p = softmax over the keys; out = p . V with V the first 512 dims
 // of each key row; lse = log sum exp of the scaled scores.
 //
-// Kernel layout: two CTAs per unit, one per half of the 512 value dims (the
-// fp32 output of 128 heads x 512 dims would fill all of tensor memory); 128
-// threads, thread t <-> head t <-> tensor-memory lane t.  Q stays in shared
-// memory for the whole unit; keys stream in blocks of 32: S = Q K^T (M 128,
-// N 32, K 576) into tensor memory, an online softmax per head (the reference
-// maximum is raised, and the accumulator rescaled, only when a block's maximum
-// exceeds it by more than 2^8, so rescales are rare), P (bf16) to shared
-// memory, O += P V (M 128, N 256, K 32) with V read in place from the key
-// block as an MN-major operand.  The next block's rows are loaded into
-// registers while the current block's products run.
+// Kernel layout: a cluster of two CTAs per unit, keys in blocks of 64.  Tensor memory (512 columns
+// of 128 fp32 lanes) holds at most half of the 128 x 512 fp32 output, so CTA
+// h owns value dims [256h, 256h + 256) and, to split the score product too,
+// score dims [288h, 288h + 288): per block of 64 keys each CTA computes a
+// partial S over its 288 dims, the two partials are exchanged through
+// distributed shared memory (st.async, completing on the receiver's mbarrier)
+// and summed -- in the same fp32 addition on both sides, so both CTAs hold
+// bit-identical scores and run the same softmax.  Each CTA thus reads only a
+// 640-byte window of every key row (dims [256h, 256h + 320) cover both its
+// score and value dims) and no product is computed twice.
+//
+// Warp roles (192 threads): warps 0-3 the softmax warpgroup (thread t <->
+// head t <-> tensor-memory lane t: partial-score exchange, online softmax with
+// a lazily raised reference maximum -- the accumulator is rescaled only when
+// a block's maximum exceeds it by more than 2^8 --, P to shared memory,
+// epilogue); one thread of warp 4 issues the MMAs, in whichever of the two
+// streams (S of a later block, O += P V of the oldest) is ready first; one
+// thread of warp 5 gathers the key rows of each block into a ring of
+// shared-memory stages with TMA (tile::gather4: four rows by 64 dims per copy,
+// 128-byte swizzle; a masked slot is an out-of-range row, which reads zeros).
+// Q (this CTA's 288 score dims) sits in tensor memory as the A operand of
+// S = Q K^T, so shared-memory bandwidth goes to the keys alone; the swizzled
+// key stage is both the K-major B of S and, read as MN-major, the V of
+// O += P V.  Every wait is bounded: a timeout sets the sticky device error
+// bit and the CTA winds down.
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -33,27 +49,32 @@ namespace skv {
 namespace {
 
 constexpr int kTcThreads = 128;              // one warpgroup: thread t <-> TMEM lane t <-> row t
-constexpr uint32_t kMaxPolls = 1u << 22;     // bound of every mbarrier wait
+constexpr uint32_t kMaxPolls = 1u << 22;     // bound of every spinning mbarrier wait
+constexpr uint32_t kMaxSleepPolls = 1u << 20; // bound of a wait whose polls may each sleep (about 2 s)
 
 // D[128][N] = A[128][K] * B^T through shared memory and tensor memory; B is
-// [N][K] row-major staged K-major, or (b_mn_major) [K][N] row-major staged
-// MN-major.
+// [N][K] row-major staged K-major, or (mode bit 0) [K][N] row-major staged
+// MN-major; A is staged K-major in shared memory, or (mode bit 1) written to
+// tensor memory (row m in lane m) and read from there by the MMA.
 __global__ void __launch_bounds__(kTcThreads) mma_selftest_kernel(const uint16_t* __restrict__ A,
                                                                   const uint16_t* __restrict__ B,
-                                                                  float* __restrict__ D, int N, int K,
-                                                                  int b_mn_major, uint32_t* __restrict__ status)
+                                                                  float* __restrict__ D, int N, int K, int mode,
+                                                                  uint32_t* __restrict__ status)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ uint64_t bar;
     __shared__ uint32_t tmem_base;
     const int tid = threadIdx.x, warp = tid >> 5;
+    const bool b_mn_major = (mode & 1) != 0, a_tmem = (mode & 2) != 0;
     uint8_t* sA = smem;
     uint8_t* sB = smem + 128 * K * 2;
     const int cpr = K / 8;
-    for (int i = tid; i < 128 * cpr; i += kTcThreads) {
-        const int r = i / cpr, c = i % cpr;
-        *reinterpret_cast<uint4*>(sA + tc::kmajor_chunk_offset(r, c, K)) =
-            *reinterpret_cast<const uint4*>(A + (size_t)r * K + c * 8);
+    if (!a_tmem) {
+        for (int i = tid; i < 128 * cpr; i += kTcThreads) {
+            const int r = i / cpr, c = i % cpr;
+            *reinterpret_cast<uint4*>(sA + tc::kmajor_chunk_offset(r, c, K)) =
+                *reinterpret_cast<const uint4*>(A + (size_t)r * K + c * 8);
+        }
     }
     if (!b_mn_major) {
         for (int i = tid; i < N * cpr; i += kTcThreads) {
@@ -71,6 +92,7 @@ __global__ void __launch_bounds__(kTcThreads) mma_selftest_kernel(const uint16_t
     }
     uint32_t ncols = 32;
     while ((int)ncols < N) ncols <<= 1;
+    if (a_tmem) ncols = 512;  // D in columns [0, N), A in [256, 256 + K / 2)
     if (warp == 0) tc::tmem_alloc(&tmem_base, ncols);
     if (tid == 0) tc::mbar_init(&bar, 1);
     tc::fence_smem_async();
@@ -78,13 +100,29 @@ __global__ void __launch_bounds__(kTcThreads) mma_selftest_kernel(const uint16_t
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t taddr = tmem_base;
+    const uint32_t tlane = taddr + ((uint32_t)(32 * warp) << 16);
+    if (a_tmem) {  // thread t writes row t of A: two bf16 per column, in memory order
+        const uint32_t* row = reinterpret_cast<const uint32_t*>(A + (size_t)tid * K);
+        for (int c0 = 0; c0 < K / 2; c0 += 8) {
+            uint32_t w[8];
+            for (int j = 0; j < 8; ++j) w[j] = row[c0 + j];
+            tc::tmem_st8_async(tlane + 256u + (uint32_t)c0, w);
+        }
+        tc::tmem_wait_st();
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+    }
     if (tid == 0) {
         const uint32_t idesc = tc::idesc_bf16_f32(128, (uint32_t)N, b_mn_major ? 1u : 0u);
         const uint32_t sbo_mn = (uint32_t)N / 8 * 128u;  // 8-k-row group stride of the MN-major B
         for (int s = 0; s < K / 16; ++s) {
             const uint64_t bdesc = b_mn_major ? tc::mnmajor_desc(tc::smem_u32(sB) + 2u * sbo_mn * s, sbo_mn)
                                               : tc::kmajor_desc(tc::smem_u32(sB) + 256u * s, K);
-            tc::mma_bf16(taddr, tc::kmajor_desc(tc::smem_u32(sA) + 256u * s, K), bdesc, idesc, s > 0 ? 1u : 0u);
+            if (a_tmem)
+                tc::mma_bf16_ta(taddr, taddr + 256u + 8u * s, bdesc, idesc, s > 0 ? 1u : 0u);
+            else
+                tc::mma_bf16(taddr, tc::kmajor_desc(tc::smem_u32(sA) + 256u * s, K), bdesc, idesc, s > 0 ? 1u : 0u);
         }
         tc::mma_commit(&bar);
     }
@@ -93,7 +131,7 @@ __global__ void __launch_bounds__(kTcThreads) mma_selftest_kernel(const uint16_t
     if (ok) {
         for (int c0 = 0; c0 < N; c0 += 32) {
             float v[32];
-            tc::tmem_ld32(taddr + ((uint32_t)(32 * warp) << 16) + (uint32_t)c0, v);
+            tc::tmem_ld32(tlane + (uint32_t)c0, v);
             for (int j = 0; j < 32 && c0 + j < N; ++j) D[(size_t)tid * N + c0 + j] = v[j];
         }
     } else if (tid == 0) {
@@ -106,214 +144,452 @@ __global__ void __launch_bounds__(kTcThreads) mma_selftest_kernel(const uint16_t
 
 constexpr int kHeads = 128;      // M of every product: one head per tensor-memory lane
 constexpr int kDim = 576;        // q / key row length (bf16)
+constexpr int kRowBytes = kDim * 2;
 constexpr int kVHalf = 256;      // value dims per CTA (of 512)
-constexpr int kBlk = 32;         // keys per block
-constexpr int kChunks = kDim / 8;                       // 16-byte chunks per row (72)
-constexpr int kPre = kBlk * kChunks / kTcThreads;       // prefetched chunks per thread (18)
-constexpr uint32_t kSmemQ = kHeads * kDim * 2;          // 147456
-constexpr uint32_t kSmemK = kBlk * kDim * 2;            // 36864
-constexpr uint32_t kSmemP = kHeads * kBlk * 2;          // 8192
+constexpr int kQKHalf = kDim / 2;                        // score dims per CTA (288)
+constexpr int kBlk = 64;         // keys per block (the N of S = Q K^T)
+constexpr int kHalfBlk = kBlk / 2;                       // keys per softmax warpgroup
+constexpr int kWinBoxes = 5;     // 64-dim column boxes of the key-row window a CTA loads (320 dims)
+constexpr int kMaxStages = 3;    // key stages in flight (2 when the slot list needs the room)
+constexpr int kSoftmaxThreads = 256;                     // two warpgroups: keys [0, 32) and [32, 64) of a block
+constexpr int kMmaWarp = 8, kLoadWarp0 = 9, kLoadWarps = 7;
+constexpr int kAttnThreads = (kLoadWarp0 + kLoadWarps) * 32;  // 512 (128 registers a thread)
+constexpr int kGathers = kBlk / 4 * kWinBoxes;           // four-row TMA copies per block (80)
+constexpr uint32_t kXBytes = kHeads * kBlk * 4;          // one partial score tile (fp32): 32768
+constexpr uint32_t kPBytes = kHeads * kBlk * 2;          // the P tile (bf16): 16384
+constexpr uint32_t kBoxBytes = kBlk * 128;               // one column box of a key stage: 64 rows x 128 B
+constexpr uint32_t kStageBytes = kWinBoxes * kBoxBytes;  // 40960
+constexpr uint32_t kOffP = 2 * kXBytes, kOffK = kOffP + kPBytes;  // key stages from 81920
+constexpr uint32_t kSmemLimit = 227 * 1024 - 4096;       // dynamic bytes beside the static control block
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColO = 256;              // S: 32 columns, O: 256 columns
-constexpr float kRescaleLog2 = 8.0f;                    // lazy rescale threshold (factor 256)
+constexpr uint32_t kColO = 0, kColS = 256, kColQ = 320;  // O 256, S 64, Q 144 columns
+constexpr float kRescaleLog2 = 8.0f;                     // lazy rescale threshold (factor 256)
+static_assert(kColQ + kQKHalf / 2 <= kTmemCols && kColS + kBlk <= kColQ, "tensor-memory columns");
+static_assert(kOffK + 2 * kStageBytes + kMaxTopk * 4 <= kSmemLimit, "shared memory");
 
-__device__ __forceinline__ uint16_t f2bf(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
-
-// Rows of key block starting at j0 into registers: chunk i of this thread is
-// chunk (tid + i * 128) of the block, row j = that / 72.  Masked or
-// out-of-range slots give zero rows.
-__device__ __forceinline__ void load_block(uint4 (&pre)[kPre], const uint8_t* hot_u, const int32_t* sl, int k, int S,
-                                           int j0, int tid)
+// Key stages for a slot list of k entries.
+__host__ __device__ constexpr int attend_stages(int k)
 {
-#pragma unroll
-    for (int i = 0; i < kPre; ++i) {
-        const int ci = tid + i * kTcThreads;
-        const int j = ci / kChunks, c = ci - j * kChunks;
-        const int key = j0 + j;
-        const int32_t slot = key < k ? sl[key] : -1;
-        pre[i] = (slot >= 0 && slot < S)
-                     ? *reinterpret_cast<const uint4*>(hot_u + (size_t)slot * (kDim * 2) + c * 16)
-                     : make_uint4(0, 0, 0, 0);
+    return kOffK + kMaxStages * kStageBytes + (uint32_t)k * 4u <= kSmemLimit ? kMaxStages : 2;
+}
+
+// Two floats to a bf16 pair (lo in the low half), round to nearest even.
+__device__ __forceinline__ uint32_t bf2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+// 2^x on the special-function unit (approximate, denormal results flush to
+// zero; -inf gives 0).  The softmax feeds it x <= 8.
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+struct AttnCtl {
+    uint64_t full[kMaxStages];   // key stage landed (TMA transaction bytes; one arrive per loader)
+    uint64_t empty[kMaxStages];  // key stage consumed by its last product
+    uint64_t s_full;             // partial S of the next block is in tensor memory
+    uint64_t s_empty;            // the softmax warpgroups have read it
+    uint64_t x_full[2];          // the peer's partial S of a block has arrived (32768 transaction bytes)
+    uint64_t m_full[2];          // both warpgroups' partial row maxima of a block are in `mpart`
+    uint64_t p_full;             // P of the block is in shared memory
+    uint64_t pv_done;            // O += P V of the block has completed
+    uint64_t q_ready;            // Q is in tensor memory
+    uint64_t fin;                // every MMA this CTA issued has completed
+    float mpart[2][2][kHeads];   // [block parity][warpgroup][head] partial row maxima of the raw scores
+    float lpart[2][kHeads];      // [warpgroup][head] partial softmax denominators
+    uint32_t tmem_base;
+    uint32_t abort;              // a wait of this CTA gave up
+};
+
+// Bounded wait on a phase of a local mbarrier, giving up early once the CTA
+// has aborted.  (A cluster-scope acquire here would cost several hundred
+// cycles per wait; the peer's data arrives as transaction bytes on the local
+// barrier, which a CTA-scope acquire observes.)
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, const volatile uint32_t* abort)
+{
+    const uint32_t a = tc::smem_u32(bar);
+    for (uint32_t i = 0; i < kMaxSleepPolls; ++i) {
+        if (tc::mbar_test(a, parity)) return true;
+        if ((i & 7u) == 7u && *abort) return false;
+    }
+    return false;
+}
+
+__device__ __forceinline__ void give_up(AttnCtl& c, uint32_t* err)
+{
+    if (!c.abort) {
+        c.abort = 1u;
+        atomicOr(err, DEVERR_TIMEOUT);
     }
 }
 
-__global__ void __launch_bounds__(kTcThreads, 1) attend_kernel(Dev d, const int32_t* __restrict__ req_ids,
-                                                               const uint16_t* __restrict__ q,
-                                                               const int32_t* __restrict__ slots,
-                                                               uint16_t* __restrict__ out, float* __restrict__ lse,
-                                                               float scale_log2)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
+    attend_kernel(const __grid_constant__ CUtensorMap hot_map, Dev d, const int32_t* __restrict__ req_ids,
+                  const uint16_t* __restrict__ q, const int32_t* __restrict__ slots, uint16_t* __restrict__ out,
+                  float* __restrict__ lse, float scale_log2, int nst)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
-    __shared__ uint64_t bar;
-    __shared__ uint32_t tmem_base;
-    __shared__ int32_t valid[kBlk];
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int uc = blockIdx.x >> 1, vh = blockIdx.x & 1;  // unit of the call, value half
+    __shared__ AttnCtl c;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int uc = blockIdx.x >> 1;                        // unit of the call
+    const uint32_t h = blockIdx.x & 1u, peer = h ^ 1u;     // rank in the cluster = value / score half
     const int b = d.layer_sel >= 0 ? uc : uc / d.L;
     const int l = d.layer_sel >= 0 ? d.layer_sel : uc % d.L;
     const int32_t r = req_ids[b];
     const int k = d.k, S = d.S;
-    uint16_t* out_u = out + ((size_t)uc * kHeads + tid) * 512 + vh * kVHalf;
-    if (r < 0 || r >= d.R) {  // not a request: zero output (assemble would have rejected it)
-        for (int c = 0; c < kVHalf; c += 8) *reinterpret_cast<uint4*>(out_u + c) = make_uint4(0, 0, 0, 0);
-        if (vh == 0 && lse) lse[(size_t)uc * kHeads + tid] = -INFINITY;
+    if (r < 0 || r >= d.R) {  // not a request: zero output (assemble would have rejected it); both CTAs leave
+        if (tid < kHeads) {
+            uint16_t* o = out + ((size_t)uc * kHeads + tid) * 512 + h * kVHalf;
+            for (int cc = 0; cc < kVHalf; cc += 8) *reinterpret_cast<uint4*>(o + cc) = make_uint4(0, 0, 0, 0);
+            if (h == 0 && lse) lse[(size_t)uc * kHeads + tid] = -INFINITY;
+        }
         return;
     }
-    const uint8_t* hot_u = d.hot + (size_t)((int64_t)r * d.L + l) * S * (kDim * 2);
+    if (tc::smem_u32(smem) & 1023u) {  // the swizzled key stages need 1024-byte-aligned rows of atoms
+        if (tid == 0) atomicOr(&d.ctl[CTL_ERR], DEVERR_TIMEOUT);
+        return;  // both CTAs of the cluster see the same layout and leave together
+    }
     const int32_t* sl = slots + (size_t)uc * k;
-    uint8_t* sQ = smem;
-    uint8_t* sK = smem + kSmemQ;
-    uint8_t* sP = sK + kSmemK;
-
-    // Q of this unit, K-major
-    const uint16_t* q_u = q + (size_t)uc * kHeads * kDim;
-    for (int i = tid; i < kHeads * kChunks; i += kTcThreads) {
-        const int h = i / kChunks, c = i - h * kChunks;
-        *reinterpret_cast<uint4*>(sQ + tc::kmajor_chunk_offset(h, c, kDim)) =
-            *reinterpret_cast<const uint4*>(q_u + (size_t)h * kDim + c * 8);
-    }
-    if (warp == 0) tc::tmem_alloc(&tmem_base, kTmemCols);
-    if (tid == 0) tc::mbar_init(&bar, 1);
-    uint4 pre[kPre];
-    load_block(pre, hot_u, sl, k, S, 0, tid);
-    tc::fence_smem_async();
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    const uint32_t tbase = tmem_base;
-    const uint32_t tlane = tbase + ((uint32_t)(32 * warp) << 16);
-    const uint32_t idesc_s = tc::idesc_bf16_f32(kHeads, kBlk, 0);
-    const uint32_t idesc_o = tc::idesc_bf16_f32(kHeads, kVHalf, 1);
-    const uint32_t aQ = tc::smem_u32(sQ), aK = tc::smem_u32(sK), aP = tc::smem_u32(sP);
-    const uint32_t kgroup = kDim / 8 * 128;  // 8-key group stride of the key block (9216 B)
-
-    float m_ref = -INFINITY;  // reference maximum (log2 domain) the exponentials use
-    float l_run = 0.0f;
-    uint32_t phase = 0;
-    bool ok = true;
     const int nblk = (k + kBlk - 1) / kBlk;
-    for (int blk = 0; blk < nblk && ok; ++blk) {
-        const int j0 = blk * kBlk;
-#pragma unroll
-        for (int i = 0; i < kPre; ++i) {
-            const int ci = tid + i * kTcThreads;
-            const int j = ci / kChunks, c = ci - j * kChunks;
-            *reinterpret_cast<uint4*>(sK + tc::kmajor_chunk_offset(j, c, kDim)) = pre[i];
-        }
-        if (tid < kBlk) {
-            const int key = j0 + tid;
-            const int32_t slot = key < k ? sl[key] : -1;
-            valid[tid] = slot >= 0 && slot < S;
-        }
-        tc::fence_smem_async();
-        tc::fence_before_sync();
-        __syncthreads();
-        tc::fence_after_sync();
-        if (blk + 1 < nblk) load_block(pre, hot_u, sl, k, S, j0 + kBlk, tid);  // in flight during the products
+    uint8_t* sX = smem;
+    uint8_t* sP = smem + kOffP;
+    uint8_t* sK = smem + kOffK;
+    int32_t* sSl = reinterpret_cast<int32_t*>(sK + nst * kStageBytes);  // slots of the unit, -1 where masked
+    volatile uint32_t* abort = &c.abort;
 
-        // S = Q K^T
-        if (tid == 0) {
-            for (int s = 0; s < kDim / 16; ++s)
-                tc::mma_bf16(tbase + kColS, tc::kmajor_desc(aQ + 256u * s, kDim), tc::kmajor_desc(aK + 256u * s, kDim),
-                             idesc_s, s > 0 ? 1u : 0u);
-            tc::mma_commit(&bar);
-        }
-        ok = __syncthreads_and(tc::mbar_wait(&bar, phase, kMaxPolls));  // one decision for the whole CTA
-        phase ^= 1u;
-        tc::fence_after_sync();
-        if (!ok) break;
-        float sv[32];
-        tc::tmem_ld32(tlane + kColS, sv);
-
-        // online softmax of this head over the block
-        float mb = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < kBlk; ++j) {
-            sv[j] = valid[j] ? sv[j] * scale_log2 : -INFINITY;
-            mb = fmaxf(mb, sv[j]);
-        }
-        float factor = 1.0f;
-        if (mb > m_ref + kRescaleLog2) {
-            factor = m_ref == -INFINITY ? 0.0f : exp2f(m_ref - mb);
-            m_ref = mb;
-            l_run *= factor;
-        }
-        if (blk > 0 && __any_sync(0xFFFFFFFFu, factor != 1.0f)) {  // rescale this warp's rows of O
-            for (int c0 = 0; c0 < kVHalf; c0 += 32) {
-                float ov[32];
-                tc::tmem_ld32(tlane + kColO + c0, ov);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) ov[j] *= factor;
-                tc::tmem_st32(tlane + kColO + c0, ov);
-            }
-        }
-        float psum = 0.0f;
-        uint32_t pk[kBlk / 2];
-#pragma unroll
-        for (int j = 0; j < kBlk; j += 2) {
-            const float p0 = sv[j] == -INFINITY ? 0.0f : exp2f(sv[j] - m_ref);
-            const float p1 = sv[j + 1] == -INFINITY ? 0.0f : exp2f(sv[j + 1] - m_ref);
-            psum += p0 + p1;
-            pk[j / 2] = (uint32_t)f2bf(p0) | ((uint32_t)f2bf(p1) << 16);
-        }
-        l_run += psum;
-#pragma unroll
-        for (int c = 0; c < kBlk / 8; ++c)
-            *reinterpret_cast<uint4*>(sP + tc::kmajor_chunk_offset(tid, c, kBlk)) =
-                make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-        tc::fence_smem_async();
-        tc::fence_before_sync();
-        __syncthreads();
-        tc::fence_after_sync();
-
-        // O += P V, V = dims [vh*256, vh*256 + 256) of the key block, MN-major
-        if (tid == 0) {
-            for (int s = 0; s < kBlk / 16; ++s)
-                tc::mma_bf16(tbase + kColO, tc::kmajor_desc(aP + 256u * s, kBlk),
-                             tc::mnmajor_desc(aK + (uint32_t)vh * (kVHalf / 8) * 128u + 2u * kgroup * s, kgroup),
-                             idesc_o, (blk > 0 || s > 0) ? 1u : 0u);
-            tc::mma_commit(&bar);
-        }
-        ok = __syncthreads_and(tc::mbar_wait(&bar, phase, kMaxPolls));
-        phase ^= 1u;
-        tc::fence_after_sync();
+    for (int i = tid; i < k; i += kAttnThreads) {
+        const int32_t slot = sl[i];
+        sSl[i] = slot >= 0 && slot < S ? slot : -1;
     }
-
-    if (ok) {
-        const float inv = l_run > 0.0f ? 1.0f / l_run : 0.0f;
-        for (int c0 = 0; c0 < kVHalf; c0 += 32) {
-            float ov[32];
-            tc::tmem_ld32(tlane + kColO + c0, ov);
-            uint32_t w[16];
-#pragma unroll
-            for (int j = 0; j < 32; j += 2) w[j / 2] = (uint32_t)f2bf(ov[j] * inv) | ((uint32_t)f2bf(ov[j + 1] * inv) << 16);
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-                *reinterpret_cast<uint4*>(out_u + c0 + 8 * c) = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+    if (tid == 0) {
+        for (int s = 0; s < kMaxStages; ++s) {
+            tc::mbar_init(&c.full[s], kLoadWarps);
+            tc::mbar_init(&c.empty[s], 1);
         }
-        if (vh == 0 && lse)
-            lse[(size_t)uc * kHeads + tid] = l_run > 0.0f ? (m_ref + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
-    } else if (tid == 0) {
-        atomicOr(&d.ctl[CTL_ERR], DEVERR_TIMEOUT);  // a product never signalled completion
+        tc::mbar_init(&c.s_full, 1);
+        tc::mbar_init(&c.s_empty, kSoftmaxThreads);
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&c.x_full[i], 1);
+            tc::mbar_init(&c.m_full[i], kSoftmaxThreads);
+        }
+        tc::mbar_init(&c.p_full, kSoftmaxThreads);
+        tc::mbar_init(&c.pv_done, 1);
+        tc::mbar_init(&c.q_ready, kSoftmaxThreads);
+        tc::mbar_init(&c.fin, 1);
+        c.abort = 0u;
+    }
+    if (warp == kMmaWarp) tc::tmem_alloc(&c.tmem_base, kTmemCols);
+    tc::fence_before_sync();
+    tc::cluster_sync();  // barriers of both CTAs exist before either sends to the other; slots staged
+    tc::fence_after_sync();
+    const uint32_t tbase = c.tmem_base;
+
+    if (warp >= kLoadWarp0) {
+        // ---- loaders: lane 0 of each of seven warps issues every seventh of a block's 80 TMA copies
+        // (four key rows x one 64-dim box of this CTA's 320-dim window; a masked slot is row -1, which
+        // reads zeros).  TMA issue is paced per warp, so the copies are spread over warps. ----
+        if (lane == 0) {
+            const int lw = warp - kLoadWarp0;
+            const int mine = (kGathers - lw + kLoadWarps - 1) / kLoadWarps;  // copies this loader issues
+            const int64_t row0 = ((int64_t)r * d.L + l) * S;                 // first hot row of this unit
+            int last[kMaxStages] = {-1, -1, -1};                              // last block issued into each stage
+            bool ok = true;
+            for (int i = 0; i < nblk; ++i) {
+                const int s = i % nst;
+                if (i >= nst && !(ok = wait_phase(&c.empty[s], ((i / nst) - 1) & 1, abort))) break;
+                tc::mbar_arrive_expect_tx(&c.full[s], (uint32_t)mine * 512u);
+                const uint32_t dst = tc::smem_u32(sK + s * kStageBytes);
+                for (int it = lw; it < kGathers; it += kLoadWarps) {
+                    const int g = it / kWinBoxes, cb = it - g * kWinBoxes;
+                    int rr[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int key = i * kBlk + 4 * g + u;
+                        const int32_t slot = key < k ? sSl[key] : -1;
+                        rr[u] = slot >= 0 ? (int)(row0 + slot) : -1;
+                    }
+                    tc::tma_gather4(dst + cb * kBoxBytes + g * 512u, &hot_map, 256 * (int)h + 64 * cb, rr[0], rr[1],
+                                    rr[2], rr[3], &c.full[s]);
+                }
+                last[s] = i;
+            }
+            if (!ok) give_up(c, &d.ctl[CTL_ERR]);
+            for (int s = 0; s < nst; ++s)  // no copy may still be landing when the CTA leaves
+                if (last[s] >= 0 && !tc::mbar_wait(&c.full[s], (uint32_t)(last[s] / nst) & 1u, kMaxPolls))
+                    give_up(c, &d.ctl[CTL_ERR]);
+        }
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        // ---- MMA issuer: whichever product is ready first.  O += P(i) V(i) as soon as P(i) is
+        // written (it frees the key stage for the loaders); S(j) as soon as its keys have landed
+        // and S(j-1) has been read out of tensor memory.  Both streams are issued in order. ----
+        if (lane == 0) {
+            const uint32_t idesc_s = tc::idesc_bf16_f32(kHeads, kBlk, 0);
+            const uint32_t idesc_o = tc::idesc_bf16_f32(kHeads, kVHalf, 1);
+            const uint32_t aK = tc::smem_u32(sK), aP = tc::smem_u32(sP);
+            bool ok = wait_phase(&c.q_ready, 0, abort);
+            tc::fence_after_sync();
+            int js = 0, ipv = 0;  // next S block, next P V block
+            uint32_t idle = 0;
+            while (ok && ipv < nblk) {
+                bool progressed = false;
+                if (ipv < js && tc::mbar_ready(tc::smem_u32(&c.p_full), (uint32_t)ipv & 1u)) {
+                    const int s = ipv % nst;
+                    tc::fence_after_sync();
+                    const uint32_t vst = aK + s * kStageBytes;  // value dims are the window's first four boxes
+#pragma unroll
+                    for (int st = 0; st < kBlk / 16; ++st)
+                        tc::mma_bf16(tbase + kColO, tc::kmajor_desc(aP + 256u * st, kBlk),
+                                     tc::sw128_mnmajor_desc(vst + 2048u * st, kBoxBytes), idesc_o,
+                                     (ipv > 0 || st > 0) ? 1u : 0u);
+                    tc::mma_commit(&c.pv_done);
+                    tc::mma_commit(&c.empty[s]);
+                    ++ipv;
+                    progressed = true;
+                }
+                if (js < nblk && tc::mbar_ready(tc::smem_u32(&c.full[js % nst]), (uint32_t)(js / nst) & 1u) &&
+                    (js == 0 || tc::mbar_ready(tc::smem_u32(&c.s_empty), (uint32_t)(js - 1) & 1u))) {
+                    const int s = js % nst;
+                    tc::fence_after_sync();
+                    const uint32_t kst = aK + s * kStageBytes;
+#pragma unroll 2
+                    for (int st = 0; st < kQKHalf / 16; ++st) {
+                        const uint32_t e = 32u * h + 16u * st;  // window dim of this step (score dims start 32 in for h = 1)
+                        tc::mma_bf16_ta(tbase + kColS, tbase + kColQ + 8u * st,
+                                        tc::sw128_kmajor_desc(kst + (e >> 6) * kBoxBytes + (e & 63u) * 2u), idesc_s,
+                                        st > 0 ? 1u : 0u);
+                    }
+                    tc::mma_commit(&c.s_full);
+                    ++js;
+                    progressed = true;
+                }
+                if (progressed) {
+                    idle = 0;
+                } else if (++idle > kMaxPolls || ((idle & 255u) == 0 && *abort)) {
+                    ok = false;
+                } else {
+                    __nanosleep(32);  // leave issue slots to the softmax warps on this sub-partition
+                }
+            }
+            if (!ok) give_up(c, &d.ctl[CTL_ERR]);
+            tc::mma_commit(&c.fin);
+            if (!tc::mbar_wait(&c.fin, 0, kMaxPolls)) give_up(c, &d.ctl[CTL_ERR]);
+        }
+        __syncwarp();
+    } else {
+        // ---- softmax: two warpgroups; warp w serves heads 32(w%4) .. +31 (its tensor-memory lane
+        // quarter) for keys [32 wg, 32 wg + 32) of every block, wg = w / 4 ----
+        const int wg = warp >> 2;
+        const int hd = ((warp & 3) << 5) | lane;  // head = tensor-memory lane
+        const uint32_t tl = tbase + ((uint32_t)((warp & 3) * 32) << 16);
+        {   // Q: this head's 288 score dims into columns [kColQ, kColQ + 144); groups of 16 columns,
+            // warpgroup 0 the first five, warpgroup 1 the other four
+            const uint4* qr = reinterpret_cast<const uint4*>(q + ((size_t)uc * kHeads + hd) * kDim + h * kQKHalf);
+            for (int g = wg * 5; g < (wg ? kQKHalf / 32 : 5); ++g) {
+                uint4 a = qr[4 * g], bq = qr[4 * g + 1], cq4 = qr[4 * g + 2], dq = qr[4 * g + 3];
+                const uint32_t w0[8] = {a.x, a.y, a.z, a.w, bq.x, bq.y, bq.z, bq.w};
+                const uint32_t w1[8] = {cq4.x, cq4.y, cq4.z, cq4.w, dq.x, dq.y, dq.z, dq.w};
+                tc::tmem_st8_async(tl + kColQ + 16u * g, w0);
+                tc::tmem_st8_async(tl + kColQ + 16u * g + 8u, w1);
+            }
+            tc::tmem_wait_st();
+            tc::fence_before_sync();
+            tc::mbar_arrive(&c.q_ready);
+        }
+        // Partial scores are exchanged one block ahead: this CTA's partial of
+        // block j is stored straight from registers into the peer's buffer
+        // j % 2 (st.async; the bytes complete on the peer's x_full[j % 2]).
+        // Block j + 1 is sent only after the peer's block j has arrived here,
+        // which the peer sends after it has read block j - 1 -- the previous
+        // user of that buffer.  Layout: [16-byte group m of 4 keys][head].
+        const uint32_t x_peer = tc::map_to_rank(tc::smem_u32(sX), peer) + (uint32_t)hd * 16u + (uint32_t)wg * 8u * 2048u;
+        const uint32_t xf0 = tc::map_to_rank(tc::smem_u32(&c.x_full[0]), peer);
+        const uint32_t xf1 = tc::map_to_rank(tc::smem_u32(&c.x_full[1]), peer);
+        // this CTA's partial S of block j, my 32 keys: tensor memory -> registers -> the peer
+        auto produce = [&](int j, float (&dst)[kHalfBlk]) -> bool {
+            if (!__all_sync(0xFFFFFFFFu, wait_phase(&c.s_full, (uint32_t)j & 1u, abort))) return false;
+            tc::fence_after_sync();
+            tc::tmem_ld32(tl + kColS + (uint32_t)(kHalfBlk * wg), dst);
+            tc::fence_before_sync();
+            tc::mbar_arrive(&c.s_empty);
+            const uint32_t xb = x_peer + (uint32_t)(j & 1) * kXBytes;
+            const uint32_t rb = (j & 1) ? xf1 : xf0;
+#pragma unroll
+            for (int m = 0; m < kHalfBlk / 4; ++m)
+                tc::st_async16(xb + 2048u * m, dst[4 * m], dst[4 * m + 1], dst[4 * m + 2], dst[4 * m + 3], rb);
+            return true;
+        };
+        float m_ref = -INFINITY;  // reference maximum (log2 domain) the exponentials use; equal in both groups
+        float l_run = 0.0f;       // this group's share of the softmax denominator
+        float cur[kHalfBlk];      // this CTA's partial S of the block being processed (my keys)
+        if (tid == 0) tc::mbar_arrive_expect_tx(&c.x_full[0], kXBytes);
+        bool ok = produce(0, cur);
+        for (int i = 0; ok && i < nblk; ++i) {
+            const int bb = i & 1;
+            if (!(ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.x_full[bb], (uint32_t)(i >> 1) & 1u, abort)))) break;
+            float sv[kHalfBlk];  // own + peer: the same fp32 sum on both CTAs
+            const uint8_t* xrow = sX + bb * kXBytes + wg * 8 * 2048 + hd * 16;
+#pragma unroll
+            for (int m = 0; m < kHalfBlk / 4; ++m) {
+                const float4 pr = *reinterpret_cast<const float4*>(xrow + 2048 * m);
+                sv[4 * m] = cur[4 * m] + pr.x;
+                sv[4 * m + 1] = cur[4 * m + 1] + pr.y;
+                sv[4 * m + 2] = cur[4 * m + 2] + pr.z;
+                sv[4 * m + 3] = cur[4 * m + 3] + pr.w;
+            }
+            if (i + 1 < nblk) {  // block i + 1 travels while this block's softmax runs
+                if (tid == 0) tc::mbar_arrive_expect_tx(&c.x_full[bb ^ 1], kXBytes);
+                if (!(ok = produce(i + 1, cur))) break;
+            }
+            // mask of my 32 keys of the block (all real in the common case)
+            const int key = i * kBlk + kHalfBlk * wg + lane;
+            const uint32_t vm = __ballot_sync(0xFFFFFFFFu, key < k && sSl[key] >= 0);
+            if (vm != 0xFFFFFFFFu) {
+#pragma unroll
+                for (int j = 0; j < kHalfBlk; ++j) sv[j] = (vm >> j) & 1u ? sv[j] : -INFINITY;
+            }
+            // row maximum of the raw scores over the block (scale > 0 keeps the order):
+            // a tree over my 32 keys, then the other group's half through shared memory
+            float mx[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                mx[j] = fmaxf(fmaxf(fmaxf(sv[j], sv[j + 4]), fmaxf(sv[j + 8], sv[j + 12])),
+                              fmaxf(fmaxf(sv[j + 16], sv[j + 20]), fmaxf(sv[j + 24], sv[j + 28])));
+            c.mpart[bb][wg][hd] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+            tc::mbar_arrive(&c.m_full[bb]);
+            if (!(ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.m_full[bb], (uint32_t)(i >> 1) & 1u, abort)))) break;
+            const float mb = fmaxf(c.mpart[bb][0][hd], c.mpart[bb][1][hd]) * scale_log2;
+            float factor = 1.0f;
+            if (mb > m_ref + kRescaleLog2) {
+                factor = m_ref == -INFINITY ? 0.0f : ex2(m_ref - mb);
+                m_ref = mb;
+                l_run *= factor;
+            }
+            if (i > 0 && __any_sync(0xFFFFFFFFu, factor != 1.0f)) {  // rescale my half of this warp's rows of O
+                if (!(ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.pv_done, (uint32_t)(i - 1) & 1u, abort)))) break;
+                tc::fence_after_sync();
+                for (int c0 = kVHalf / 2 * wg; c0 < kVHalf / 2 * (wg + 1); c0 += 32) {
+                    float ov[32];
+                    tc::tmem_ld32(tl + kColO + c0, ov);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) ov[j] *= factor;
+                    tc::tmem_st32(tl + kColO + c0, ov);
+                }
+                tc::fence_before_sync();
+            }
+            // p = 2^(s * scale - m_ref); masked keys give 2^-inf = 0.  While no
+            // real key has been seen (m_ref = -inf for every head) all p are 0.
+            uint32_t pk[kHalfBlk / 2];
+            float ps[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            if (m_ref != -INFINITY) {
+                const float neg_m = -m_ref;
+#pragma unroll
+                for (int j = 0; j < kHalfBlk; j += 2) {
+                    const float p0 = ex2(fmaf(sv[j], scale_log2, neg_m));
+                    const float p1 = ex2(fmaf(sv[j + 1], scale_log2, neg_m));
+                    ps[(j >> 1) & 3] += p0 + p1;
+                    pk[j / 2] = bf2(p0, p1);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < kHalfBlk / 2; ++j) pk[j] = 0u;
+            }
+            l_run += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+            // the P tile is free once O += P(i-1) V(i-1) has completed
+            if (i >= 1 && !(ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.pv_done, (uint32_t)(i - 1) & 1u, abort))))
+                break;
+#pragma unroll
+            for (int cc = 0; cc < kHalfBlk / 8; ++cc)
+                *reinterpret_cast<uint4*>(sP + tc::kmajor_chunk_offset(hd, 4 * wg + cc, kBlk)) =
+                    make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+            tc::fence_smem_async();
+            tc::mbar_arrive(&c.p_full);
+        }
+        if (ok && nblk > 0) ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.pv_done, (uint32_t)(nblk - 1) & 1u, abort));
+        // the denominator is the two groups' shares summed in a fixed order (the same in both)
+        c.lpart[wg][hd] = l_run;
+        tc::named_sync(1, kSoftmaxThreads);  // every softmax thread gets here, aborted or not
+        const float l_all = c.lpart[0][hd] + c.lpart[1][hd];
+        if (ok) {
+            tc::fence_after_sync();
+            uint16_t* o = out + ((size_t)uc * kHeads + hd) * 512 + h * kVHalf + kVHalf / 2 * wg;
+            const float inv = l_all > 0.0f ? 1.0f / l_all : 0.0f;
+            for (int c0 = 0; c0 < kVHalf / 2; c0 += 32) {
+                float ov[32];
+                tc::tmem_ld32(tl + kColO + kVHalf / 2 * wg + c0, ov);
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+                    *reinterpret_cast<uint4*>(o + c0 + 8 * cc) =
+                        make_uint4(bf2(ov[8 * cc] * inv, ov[8 * cc + 1] * inv), bf2(ov[8 * cc + 2] * inv, ov[8 * cc + 3] * inv),
+                                   bf2(ov[8 * cc + 4] * inv, ov[8 * cc + 5] * inv), bf2(ov[8 * cc + 6] * inv, ov[8 * cc + 7] * inv));
+            }
+            if (h == 0 && wg == 0 && lse)
+                lse[(size_t)uc * kHeads + hd] = l_all > 0.0f ? (m_ref + log2f(l_all)) * 0.69314718055994531f : -INFINITY;
+        } else {
+            give_up(c, &d.ctl[CTL_ERR]);
+        }
     }
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tbase, kTmemCols);
+    tc::cluster_sync();  // neither CTA leaves while the other may still write into its shared memory
+    if (warp == kMmaWarp) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tbase, kTmemCols);
+    }
 }
 
 }  // namespace
 
-size_t attend_smem_bytes() { return kSmemQ + kSmemK + kSmemP; }
-
-cudaError_t launch_attend(const Dev& d, const int32_t* req_ids, int B, const void* q, const int32_t* slots,
-                          void* out, float* lse, float sm_scale, cudaStream_t st)
+size_t attend_smem_bytes(int k)
 {
-    static const size_t smem = attend_smem_bytes();
-    cudaError_t e = cudaFuncSetAttribute(attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attend_kernel<<<call_units(d, B) * 2, kTcThreads, smem, st>>>(d, req_ids, static_cast<const uint16_t*>(q), slots,
-                                                                   static_cast<uint16_t*>(out), lse,
-                                                                   sm_scale * 1.4426950408889634f);
+    return kOffK + (size_t)attend_stages(k) * kStageBytes + ((size_t)k * 4 + 15) / 16 * 16;
+}
+
+// The hot buffer as a 2-D tensor of R*L*S rows by 576 bf16 (row stride 1152
+// bytes) for TMA: box one row by 64 columns, 128-byte swizzle, out-of-range
+// rows read as zeros.  cuTensorMapEncodeTiled is reached through the runtime's
+// driver entry point (no link against the driver library).
+cudaError_t encode_hot_map(const Dev& d, CUtensorMap* map)
+{
+    const uint64_t rows = (uint64_t)d.R * (uint64_t)d.L * (uint64_t)d.S;
+    if (rows > 0x7FFFFFFFull || d.row_bytes != kRowBytes) return cudaErrorInvalidValue;
+    using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                     const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                     CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+    static EncodeTiled encode = nullptr;
+    if (!encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult found = cudaDriverEntryPointSymbolNotFound;
+        const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                                               &found);
+        if (e != cudaSuccess) return e;
+        if (found != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+        encode = reinterpret_cast<EncodeTiled>(fn);
+    }
+    const cuuint64_t dims[2] = {(cuuint64_t)kDim, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)kRowBytes};
+    const cuuint32_t box[2] = {64, 1}, elem_strides[2] = {1, 1};
+    const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d.hot, dims, strides, box, elem_strides,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t launch_attend(const void* hot_map, const Dev& d, const int32_t* req_ids, int B, const void* q,
+                          const int32_t* slots, void* out, float* lse, float sm_scale, cudaStream_t st)
+{
+    static const cudaError_t attr = cudaFuncSetAttribute(attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                         (int)kSmemLimit);
+    if (attr != cudaSuccess) return attr;
+    if (d.k > (int)kMaxTopk) return cudaErrorInvalidValue;
+    attend_kernel<<<call_units(d, B) * 2, kAttnThreads, attend_smem_bytes(d.k), st>>>(
+        *static_cast<const CUtensorMap*>(hot_map), d, req_ids, static_cast<const uint16_t*>(q), slots,
+        static_cast<uint16_t*>(out), lse, sm_scale * 1.4426950408889634f, attend_stages(d.k));
     return cudaGetLastError();
 }
 
@@ -323,7 +599,8 @@ extern "C" skv_status skv_attend(skv_ctx* ctx, const int32_t* req_ids_dev, int32
                                  const int32_t* slots_dev, void* out_dev, float* lse_dev, float sm_scale,
                                  skv_stream_t stream)
 {
-    if (!ctx || B < 0 || B > ctx->cfg.max_batch || layer < -1 || layer >= ctx->cfg.num_layers)
+    if (!ctx || B < 0 || B > ctx->cfg.max_batch || layer < -1 || layer >= ctx->cfg.num_layers ||
+        !(sm_scale > 0.0f) || !std::isfinite(sm_scale))
         return SKV_ERR_INVALID_ARG;
     if (B == 0) return SKV_OK;
     if (!req_ids_dev || !q_dev || !slots_dev || !out_dev || ctx->cfg.row_bytes != skv::kDim * 2)
@@ -332,9 +609,15 @@ extern "C" skv_status skv_attend(skv_ctx* ctx, const int32_t* req_ids_dev, int32
     int prev = -1;
     if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
     if (prev != ctx->cfg.device && cudaSetDevice(ctx->cfg.device) != cudaSuccess) return SKV_ERR_CUDA;
+    cudaError_t e = cudaSuccess;
+    if (!ctx->hot_map_ready) {  // host-side encoding only: safe while a stream is being captured
+        e = skv::encode_hot_map(ctx->d, &ctx->hot_map);
+        ctx->hot_map_ready = e == cudaSuccess;
+    }
     skv::Dev d = ctx->d;
     d.layer_sel = layer;
-    const cudaError_t e = skv::launch_attend(d, req_ids_dev, B, q_dev, slots_dev, out_dev, lse_dev, sm_scale, stream);
+    if (e == cudaSuccess)
+        e = skv::launch_attend(&ctx->hot_map, d, req_ids_dev, B, q_dev, slots_dev, out_dev, lse_dev, sm_scale, stream);
     if (prev >= 0 && prev != ctx->cfg.device) cudaSetDevice(prev);
     if (e != cudaSuccess) {
         skv::set_last_error_message((std::string("skv_attend: ") + cudaGetErrorString(e)).c_str());
@@ -344,9 +627,10 @@ extern "C" skv_status skv_attend(skv_ctx* ctx, const int32_t* req_ids_dev, int32
 }
 
 extern "C" skv_status skv_selftest_mma(const void* a_dev, const void* b_dev, float* d_dev, int32_t n, int32_t k,
-                                       int32_t b_mn_major, skv_stream_t stream)
+                                       int32_t mode, skv_stream_t stream)
 {
-    if (!a_dev || !b_dev || !d_dev || n < 16 || n > 256 || n % 16 || k < 16 || k > 128 || k % 16)
+    if (!a_dev || !b_dev || !d_dev || n < 16 || n > 256 || n % 16 || k < 16 || k > 128 || k % 16 || mode < 0 ||
+        mode > 3)
         return SKV_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(a_dev) | reinterpret_cast<uintptr_t>(b_dev)) & 15u) return SKV_ERR_INVALID_ARG;
     uint32_t* status = nullptr;
@@ -357,7 +641,7 @@ extern "C" skv_status skv_selftest_mma(const void* a_dev, const void* b_dev, flo
     if (e == cudaSuccess) {
         skv::mma_selftest_kernel<<<1, skv::kTcThreads, smem, stream>>>(static_cast<const uint16_t*>(a_dev),
                                                                         static_cast<const uint16_t*>(b_dev), d_dev,
-                                                                        n, k, b_mn_major, status);
+                                                                        n, k, mode, status);
         e = cudaGetLastError();
     }
     uint32_t h = 0;

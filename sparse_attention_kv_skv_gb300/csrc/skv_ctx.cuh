@@ -3,6 +3,8 @@
 
 #include <vector>
 
+#include <cuda.h>
+
 #include "skv.h"
 #include "skv_internal.cuh"
 
@@ -20,6 +22,8 @@ struct skv_ctx {
     cudaEvent_t ev_before = nullptr, ev_after = nullptr;
     int gather_grid = 0;
     int plan_resident = 1;  // fused-kernel CTAs resident at once (L2 prefetch budget)
+    CUtensorMap hot_map{};  // TMA view of the hot buffer for the attention consumer (built on first use)
+    bool hot_map_ready = false;
 };
 
 namespace skv {

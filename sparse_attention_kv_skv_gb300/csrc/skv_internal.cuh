@@ -77,9 +77,13 @@ int plan_resident_ctas(int k, int S);
 cudaError_t prepare_step_kernels(int k, int S, int* gather_grid);
 
 // Attention over assembled slots (tensor cores).
-size_t attend_smem_bytes();
-cudaError_t launch_attend(const Dev& d, const int32_t* req_ids, int B, const void* q, const int32_t* slots,
-                          void* out, float* lse, float sm_scale, cudaStream_t st);
+size_t attend_smem_bytes(int k);
+// Builds the CUtensorMap (a 128-byte opaque struct, passed as `map`) that
+// launch_attend gathers key rows through.
+cudaError_t encode_hot_map(const Dev& d, struct CUtensorMap_st* map);
+// hot_map: a CUtensorMap over the hot buffer as [R*L*S rows][576] bf16 (box one row x 64, 128B swizzle).
+cudaError_t launch_attend(const void* hot_map, const Dev& d, const int32_t* req_ids, int B, const void* q,
+                          const int32_t* slots, void* out, float* lse, float sm_scale, cudaStream_t st);
 
 // Lifecycle kernels.
 cudaError_t launch_reset_request(const Dev& d, int r, int64_t len, int active, cudaStream_t st);

@@ -1,8 +1,9 @@
 // Blackwell (sm_100 family) tensor-core primitives used by the attention
 // consumer: shared-memory matrix descriptors, the tcgen05 MMA (bf16 x bf16 ->
 // fp32, accumulator in tensor memory), tensor-memory allocation and loads /
-// stores, and bounded mbarrier waits.  Written from the PTX ISA's description
-// of tcgen05; no vendor library code.
+// stores, bounded mbarrier waits, plus the TMA row gather and cluster (CTA
+// pair) operations the attention pipeline uses.  Written from the PTX
+// ISA's description of these instructions; no vendor library code.
 #pragma once
 
 #include <cstdint>
@@ -61,6 +62,37 @@ __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t saddr, uint32_t kgroup
     return d;
 }
 
+// 128-byte-swizzled layouts (what a TMA copy with the 128B swizzle writes):
+// rows of 128 bytes (64 bf16), the eight 16-byte chunks of row r stored at
+// chunk index c ^ (r % 8), 8-row atoms of 1024 bytes (1024-byte aligned).
+// K-major: a row is one M/N index, K runs along the row; the MMA's k-th step
+// of 16 elements starts 32 bytes further inside the row, the next 64
+// elements of K live in another region of rows.  8-row groups at 1024 bytes.
+__device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)1u << 16;                    // leading offset: unused for this layout
+    d |= (uint64_t)(1024u >> 4) << 32;          // 8-row group stride
+    d |= (uint64_t)1u << 46;
+    d |= (uint64_t)2u << 61;                    // 128-byte swizzle
+    return d;
+}
+// MN-major: a row is one K index with 64 consecutive M/N elements; regions of
+// 64 M/N elements `region` bytes apart (leading offset), 8-row K groups at
+// 1024 bytes (stride offset); the MMA's k-th step of 16 rows starts 2048
+// bytes further.
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t saddr, uint32_t region)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((region >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)(1024u >> 4) << 32;
+    d |= (uint64_t)1u << 46;
+    d |= (uint64_t)2u << 61;
+    return d;
+}
+
 // Instruction descriptor of kind::f16: D fp32, A and B bf16, no negation,
 // shape M x N (K = 16 per instruction); A K-major; B K-major, or MN-major
 // when b_mn_major.
@@ -77,6 +109,19 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
         " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// The same with A read from tensor memory: row m of A in lane m, two bf16
+// per 32-bit column (element 2c in the low half of column c); the k-th step
+// of 16 elements starts 8 columns further.
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate)
+{
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -127,10 +172,60 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32])
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// 8 consecutive 32-bit columns of this thread's lane; completes at the next
+// tmem_wait_st().
+__device__ __forceinline__ void tmem_st8_async(uint32_t taddr, const uint32_t* r)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n" ::"r"(taddr), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
 {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+// One poll of phase `parity` (acquire at CTA scope: covers this CTA's own
+// writes, the tensor core's commits and transaction bytes that completed on
+// the barrier -- including st.async data from a peer CTA).
+// The thread may sleep up to kSuspendNs inside one poll (it wakes when the
+// phase completes), so waiting warps do not take issue slots from working ones.
+constexpr uint32_t kSuspendNs = 2000;
+__device__ __forceinline__ bool mbar_test(uint32_t bar_addr, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(bar_addr), "r"(parity), "n"(kSuspendNs)
+        : "memory");
+    return done != 0;
+}
+// Non-blocking test of phase `parity` (never suspends the thread).
+__device__ __forceinline__ bool mbar_ready(uint32_t bar_addr, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(bar_addr), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+// Arrive and raise the phase's expected transaction count by `bytes`.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
 }
 
 // Wait for phase `parity` of `bar` to complete, giving up after max_polls
@@ -149,6 +244,52 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
         if (done) return true;
     }
     return false;
+}
+
+// ---- TMA row gather and the CTA pair of a cluster ----
+
+// Four rows (row ids r0..r3 of a 2-D tensor map whose box is one row of 64
+// bf16 at column x) into 512 contiguous bytes of shared memory, swizzled as
+// the map says; the bytes complete on `bar`.  A row id outside the tensor
+// (e.g. -1) reads zeros.  x * 2 must be a multiple of 16.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* map, int x, int r0, int r1, int r2, int r3,
+                                            uint64_t* bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(map), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Shared-memory address of the same variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+// 16 bytes into another CTA's shared memory; the write completes as
+// transaction bytes on that CTA's mbarrier `remote_bar`.
+__device__ __forceinline__ void st_async16(uint32_t remote_addr, float a, float b, float c, float d,
+                                           uint32_t remote_bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     remote_addr),
+                 "r"(__float_as_uint(a)), "r"(__float_as_uint(b)), "r"(__float_as_uint(c)), "r"(__float_as_uint(d)),
+                 "r"(remote_bar)
+                 : "memory");
+}
+// Named barrier `id` over `nthreads` threads (a multiple of 32); only where
+// every participating thread is certain to arrive.
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t nthreads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+// Every thread of both CTAs of the cluster.
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 }  // namespace tc

@@ -95,3 +95,32 @@ def test_attention_one_layer_and_fully_masked_units():
         assert not out[2].any() and np.all(np.isneginf(lse[2]))
     finally:
         p.close()
+
+
+@pytest.mark.parametrize("k", [20, 40])
+def test_attention_short_topk_and_non_request(k):
+    """One and two key blocks (the pipeline never fills), plus an entry whose
+    request id is not a request: zero output and lse = -inf for it."""
+    w = wl.Workload(f"attn_k{k}", B=3, L=2, ctx=700, k=k, S=64, steps=2, fresh=0.5)
+    p = Pair(w)
+    try:
+        for s in range(w.steps):
+            p.step(s)
+        units = [(b, l) for b in range(w.B) for l in range(w.L)]
+        q = _queries(w, units)
+        req = p.req_dev.clone()
+        req[1] = -1
+        out_d = torch.full((len(units), 128, 512), 0x7FC0, dtype=torch.int16, device="cuda")
+        lse_d = torch.full((len(units), 128), float("nan"), device="cuda")
+        p.ctx.attend(req, torch.from_numpy(q).cuda(), p.slots_dev, out_d, lse_d, sm_scale=0.3)
+        out = out_d.cpu().numpy().view(np.uint16)
+        lse = lse_d.cpu().numpy()
+        slots = p.slots_dev.cpu().numpy().reshape(len(units), w.k)
+        keep = [n for n, (b, _) in enumerate(units) if b != 1]
+        _check_units(p, [units[n] for n in keep], slots[keep], q[keep], out[keep], lse[keep], 0.3)
+        for n, (b, _) in enumerate(units):
+            if b == 1:
+                assert not out[n].any() and np.all(np.isneginf(lse[n]))
+        assert p.ctx.get_device_error() == 0
+    finally:
+        p.close()
