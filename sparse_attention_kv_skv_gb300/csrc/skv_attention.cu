@@ -150,27 +150,44 @@ constexpr int kQKHalf = kDim / 2;                        // score dims per CTA (
 constexpr int kBlk = 64;         // keys per block (the N of S = Q K^T)
 constexpr int kHalfBlk = kBlk / 2;                       // keys per softmax warpgroup
 constexpr int kWinBoxes = 5;     // 64-dim column boxes of the key-row window a CTA loads (320 dims)
-constexpr int kMaxStages = 3;    // key stages in flight (2 when the slot list needs the room)
+constexpr int kMaxStages = 4;    // key stages in flight (3 when a long slot list needs the room)
 constexpr int kSoftmaxThreads = 256;                     // two warpgroups: keys [0, 32) and [32, 64) of a block
 constexpr int kMmaWarp = 8, kLoadWarp0 = 9, kLoadWarps = 7;
-constexpr int kAttnThreads = (kLoadWarp0 + kLoadWarps) * 32;  // 512 (128 registers a thread)
+constexpr int kAttnThreads = (kLoadWarp0 + kLoadWarps) * 32;  // 512 (128 registers a thread at launch)
+constexpr int kSoftmaxRegs = 168, kServiceRegs = 88;     // after the split (see the kernel)
+static_assert(kSoftmaxThreads * kSoftmaxRegs + (kAttnThreads - kSoftmaxThreads) * kServiceRegs ==
+                  kAttnThreads * (65536 / kAttnThreads),
+              "the register split must add up to the launch's registers");
 constexpr int kGathers = kBlk / 4 * kWinBoxes;           // four-row TMA copies per block (80)
 constexpr uint32_t kXBytes = kHeads * kBlk * 4;          // one partial score tile (fp32): 32768
-constexpr uint32_t kPBytes = kHeads * kBlk * 2;          // the P tile (bf16): 16384
 constexpr uint32_t kBoxBytes = kBlk * 128;               // one column box of a key stage: 64 rows x 128 B
 constexpr uint32_t kStageBytes = kWinBoxes * kBoxBytes;  // 40960
-constexpr uint32_t kOffP = 2 * kXBytes, kOffK = kOffP + kPBytes;  // key stages from 81920
-constexpr uint32_t kSmemLimit = 227 * 1024 - 4096;       // dynamic bytes beside the static control block
+constexpr uint32_t kSmemLimit = 227 * 1024;              // dynamic shared memory a CTA may have (no static part)
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 0, kColS = 256, kColQ = 320;  // O 256, S 64, Q 144 columns
+constexpr uint32_t kColO = 0, kColS = 256, kColQ = 320, kColP = 464;  // O 256, S 64, Q 144, P 32 columns
 constexpr float kRescaleLog2 = 8.0f;                     // lazy rescale threshold (factor 256)
-static_assert(kColQ + kQKHalf / 2 <= kTmemCols && kColS + kBlk <= kColQ, "tensor-memory columns");
-static_assert(kOffK + 2 * kStageBytes + kMaxTopk * 4 <= kSmemLimit, "shared memory");
+static_assert(kColQ + kQKHalf / 2 <= kColP && kColP + kBlk / 2 <= kTmemCols && kColS + kBlk <= kColQ,
+              "tensor-memory columns");
 
-// Key stages for a slot list of k entries.
-__host__ __device__ constexpr int attend_stages(int k)
+struct alignas(16) AttnCtl;
+// Shared-memory layout for a slot list of k entries: the key stages first
+// (1024-byte aligned for the swizzle), then the two exchange tiles, the
+// per-block masks of real keys (two words a block) and the control block.
+struct AttnLayout {
+    int stages;
+    uint32_t off_x, off_mask, off_ctl, bytes;
+};
+__host__ __device__ constexpr uint32_t attend_ctl_bytes();
+__host__ __device__ inline AttnLayout attend_layout(int k)
 {
-    return kOffK + kMaxStages * kStageBytes + (uint32_t)k * 4u <= kSmemLimit ? kMaxStages : 2;
+    const uint32_t masks = (uint32_t)((k + kBlk - 1) / kBlk) * 8u;
+    for (int st = kMaxStages;; --st) {
+        AttnLayout a{st, (uint32_t)st * kStageBytes, 0, 0, 0};
+        a.off_mask = a.off_x + 2 * kXBytes;
+        a.off_ctl = (a.off_mask + masks + 15u) & ~15u;
+        a.bytes = a.off_ctl + attend_ctl_bytes();
+        if (a.bytes <= kSmemLimit || st == 2) return a;
+    }
 }
 
 // Two floats to a bf16 pair (lo in the low half), round to nearest even.
@@ -189,22 +206,23 @@ __device__ __forceinline__ float ex2(float x)
     return y;
 }
 
-struct AttnCtl {
+struct alignas(16) AttnCtl {
     uint64_t full[kMaxStages];   // key stage landed (TMA transaction bytes; one arrive per loader)
     uint64_t empty[kMaxStages];  // key stage consumed by its last product
     uint64_t s_full;             // partial S of the next block is in tensor memory
     uint64_t s_empty;            // the softmax warpgroups have read it
     uint64_t x_full[2];          // the peer's partial S of a block has arrived (32768 transaction bytes)
     uint64_t m_full[2];          // both warpgroups' partial row maxima of a block are in `mpart`
-    uint64_t p_full;             // P of the block is in shared memory
+    uint64_t p_full;             // P of the block is in tensor memory
     uint64_t pv_done;            // O += P V of the block has completed
     uint64_t q_ready;            // Q is in tensor memory
     uint64_t fin;                // every MMA this CTA issued has completed
     float mpart[2][2][kHeads];   // [block parity][warpgroup][head] partial row maxima of the raw scores
-    float lpart[2][kHeads];      // [warpgroup][head] partial softmax denominators
     uint32_t tmem_base;
     uint32_t abort;              // a wait of this CTA gave up
 };
+__host__ __device__ constexpr uint32_t attend_ctl_bytes() { return (uint32_t)sizeof(AttnCtl); }
+static_assert(sizeof(AttnCtl) % 16 == 0, "control block alignment");
 
 // Bounded wait on a phase of a local mbarrier, giving up early once the CTA
 // has aborted.  (A cluster-scope acquire here would cost several hundred
@@ -231,10 +249,11 @@ __device__ __forceinline__ void give_up(AttnCtl& c, uint32_t* err)
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
     attend_kernel(const __grid_constant__ CUtensorMap hot_map, Dev d, const int32_t* __restrict__ req_ids,
                   const uint16_t* __restrict__ q, const int32_t* __restrict__ slots, uint16_t* __restrict__ out,
-                  float* __restrict__ lse, float scale_log2, int nst)
+                  float* __restrict__ lse, float scale_log2, AttnLayout lay)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
-    __shared__ AttnCtl c;
+    AttnCtl& c = *reinterpret_cast<AttnCtl*>(smem + lay.off_ctl);
+    const int nst = lay.stages;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int uc = blockIdx.x >> 1;                        // unit of the call
     const uint32_t h = blockIdx.x & 1u, peer = h ^ 1u;     // rank in the cluster = value / score half
@@ -256,15 +275,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
     }
     const int32_t* sl = slots + (size_t)uc * k;
     const int nblk = (k + kBlk - 1) / kBlk;
-    uint8_t* sX = smem;
-    uint8_t* sP = smem + kOffP;
-    uint8_t* sK = smem + kOffK;
-    int32_t* sSl = reinterpret_cast<int32_t*>(sK + nst * kStageBytes);  // slots of the unit, -1 where masked
+    uint8_t* sK = smem;  // key stages
+    uint8_t* sX = smem + lay.off_x;
+    uint32_t* sMask = reinterpret_cast<uint32_t*>(smem + lay.off_mask);  // bit j of word 2i + g: key 64i + 32g + j is real
     volatile uint32_t* abort = &c.abort;
 
-    for (int i = tid; i < k; i += kAttnThreads) {
-        const int32_t slot = sl[i];
-        sSl[i] = slot >= 0 && slot < S ? slot : -1;
+    for (int g = warp; g < 2 * nblk; g += kAttnThreads / 32) {
+        const int key = 32 * g + lane;
+        const int32_t slot = key < k ? sl[key] : -1;
+        const uint32_t m = __ballot_sync(0xFFFFFFFFu, slot >= 0 && slot < S);
+        if (lane == 0) sMask[g] = m;
     }
     if (tid == 0) {
         for (int s = 0; s < kMaxStages; ++s) {
@@ -285,103 +305,125 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
     }
     if (warp == kMmaWarp) tc::tmem_alloc(&c.tmem_base, kTmemCols);
     tc::fence_before_sync();
-    tc::cluster_sync();  // barriers of both CTAs exist before either sends to the other; slots staged
+    tc::cluster_sync();  // barriers of both CTAs exist before either sends to the other; masks staged
     tc::fence_after_sync();
     const uint32_t tbase = c.tmem_base;
+    // Register split (warpgroup-wide): the two softmax warpgroups take 168 a thread, the MMA and
+    // loader warpgroups give theirs down to 88 -- 256 x 168 + 256 x 88 = 512 x 128, the launch's
+    // total, and per SM sub-partition 2 x 168 + 2 x 88 = 4 x 128 as well.
 
-    if (warp >= kLoadWarp0) {
-        // ---- loaders: lane 0 of each of seven warps issues every seventh of a block's 80 TMA copies
-        // (four key rows x one 64-dim box of this CTA's 320-dim window; a masked slot is row -1, which
-        // reads zeros).  TMA issue is paced per warp, so the copies are spread over warps. ----
-        if (lane == 0) {
+    if (warp >= kMmaWarp) {
+        tc::regs_shrink<kServiceRegs>();
+        if (warp >= kLoadWarp0) {
+            // ---- loaders: seven warps share a block's 80 TMA copies (four key rows x one 64-dim box of
+            // this CTA's 320-dim window; a masked slot is row -1, which reads zeros), lane j of warp w
+            // issuing copy w + 7j -- TMA issue is paced per issuing thread, so the copies are spread over
+            // as many lanes and warps as possible.  The warp fetches a block's 64 slots one block ahead
+            // (two a lane) and passes each lane its four rows by shuffle. ----
             const int lw = warp - kLoadWarp0;
-            const int mine = (kGathers - lw + kLoadWarps - 1) / kLoadWarps;  // copies this loader issues
-            const int64_t row0 = ((int64_t)r * d.L + l) * S;                 // first hot row of this unit
-            int last[kMaxStages] = {-1, -1, -1};                              // last block issued into each stage
+            const uint32_t mine = (uint32_t)((kGathers - lw + kLoadWarps - 1) / kLoadWarps);  // copies this loader issues
+            const int64_t row0 = ((int64_t)r * d.L + l) * S;                                 // first hot row of this unit
+            auto fetch = [&](int i, int half) -> int32_t {
+                const int key = i * kBlk + 32 * half + lane;
+                const int32_t slot = key < k ? sl[key] : -1;
+                return slot >= 0 && slot < S ? slot : -1;
+            };
+            int32_t v0 = fetch(0, 0), v1 = fetch(0, 1);
+            int last[kMaxStages] = {-1, -1, -1, -1};  // last block issued into each stage
             bool ok = true;
             for (int i = 0; i < nblk; ++i) {
                 const int s = i % nst;
-                if (i >= nst && !(ok = wait_phase(&c.empty[s], ((i / nst) - 1) & 1, abort))) break;
-                tc::mbar_arrive_expect_tx(&c.full[s], (uint32_t)mine * 512u);
-                const uint32_t dst = tc::smem_u32(sK + s * kStageBytes);
-                for (int it = lw; it < kGathers; it += kLoadWarps) {
+                if (i >= nst && !(ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.empty[s], ((i / nst) - 1) & 1, abort))))
+                    break;
+                const int32_t n0 = i + 1 < nblk ? fetch(i + 1, 0) : -1, n1 = i + 1 < nblk ? fetch(i + 1, 1) : -1;
+                if (lane == 0) tc::mbar_arrive_expect_tx(&c.full[s], mine * 512u);
+                __syncwarp();
+                {   // lane j issues copy lw + 7j: one warp instruction for all of this warp's copies
+                    const int it = lw + kLoadWarps * lane;
                     const int g = it / kWinBoxes, cb = it - g * kWinBoxes;
                     int rr[4];
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
-                        const int key = i * kBlk + 4 * g + u;
-                        const int32_t slot = key < k ? sSl[key] : -1;
+                        const int j = (4 * g + u) & (kBlk - 1);  // key of the block
+                        const int32_t a = __shfl_sync(0xFFFFFFFFu, v0, j & 31), b2 = __shfl_sync(0xFFFFFFFFu, v1, j & 31);
+                        const int32_t slot = j < 32 ? a : b2;
                         rr[u] = slot >= 0 ? (int)(row0 + slot) : -1;
                     }
-                    tc::tma_gather4(dst + cb * kBoxBytes + g * 512u, &hot_map, 256 * (int)h + 64 * cb, rr[0], rr[1],
-                                    rr[2], rr[3], &c.full[s]);
+                    if ((uint32_t)lane < mine)
+                        tc::tma_gather4(tc::smem_u32(sK + s * kStageBytes) + cb * kBoxBytes + g * 512u, &hot_map,
+                                        256 * (int)h + 64 * cb, rr[0], rr[1], rr[2], rr[3], &c.full[s]);
                 }
                 last[s] = i;
+                v0 = n0;
+                v1 = n1;
             }
-            if (!ok) give_up(c, &d.ctl[CTL_ERR]);
-            for (int s = 0; s < nst; ++s)  // no copy may still be landing when the CTA leaves
-                if (last[s] >= 0 && !tc::mbar_wait(&c.full[s], (uint32_t)(last[s] / nst) & 1u, kMaxPolls))
-                    give_up(c, &d.ctl[CTL_ERR]);
-        }
-        __syncwarp();
-    } else if (warp == kMmaWarp) {
-        // ---- MMA issuer: whichever product is ready first.  O += P(i) V(i) as soon as P(i) is
-        // written (it frees the key stage for the loaders); S(j) as soon as its keys have landed
-        // and S(j-1) has been read out of tensor memory.  Both streams are issued in order. ----
-        if (lane == 0) {
-            const uint32_t idesc_s = tc::idesc_bf16_f32(kHeads, kBlk, 0);
-            const uint32_t idesc_o = tc::idesc_bf16_f32(kHeads, kVHalf, 1);
-            const uint32_t aK = tc::smem_u32(sK), aP = tc::smem_u32(sP);
-            bool ok = wait_phase(&c.q_ready, 0, abort);
-            tc::fence_after_sync();
-            int js = 0, ipv = 0;  // next S block, next P V block
-            uint32_t idle = 0;
-            while (ok && ipv < nblk) {
-                bool progressed = false;
-                if (ipv < js && tc::mbar_ready(tc::smem_u32(&c.p_full), (uint32_t)ipv & 1u)) {
-                    const int s = ipv % nst;
-                    tc::fence_after_sync();
-                    const uint32_t vst = aK + s * kStageBytes;  // value dims are the window's first four boxes
+            if (lane == 0) {
+                if (!ok) give_up(c, &d.ctl[CTL_ERR]);
+                for (int s = 0; s < nst; ++s)  // no copy may still be landing when the CTA leaves
+                    if (last[s] >= 0 && !tc::mbar_wait(&c.full[s], (uint32_t)(last[s] / nst) & 1u, kMaxPolls))
+                        give_up(c, &d.ctl[CTL_ERR]);
+            }
+            __syncwarp();
+        } else {
+            // ---- MMA issuer: whichever product is ready first.  O += P(i) V(i) as soon as P(i) is
+            // written (it frees the key stage for the loaders); S(j) as soon as its keys have landed
+            // and S(j-1) has been read out of tensor memory.  Both streams are issued in order. ----
+            if (lane == 0) {
+                const uint32_t idesc_s = tc::idesc_bf16_f32(kHeads, kBlk, 0);
+                const uint32_t idesc_o = tc::idesc_bf16_f32(kHeads, kVHalf, 1);
+                const uint32_t aK = tc::smem_u32(sK);
+                bool ok = wait_phase(&c.q_ready, 0, abort);
+                tc::fence_after_sync();
+                int js = 0, ipv = 0;  // next S block, next P V block
+                uint32_t idle = 0;
+                while (ok && ipv < nblk) {
+                    bool progressed = false;
+                    if (ipv < js && tc::mbar_ready(tc::smem_u32(&c.p_full), (uint32_t)ipv & 1u)) {
+                        const int s = ipv % nst;
+                        tc::fence_after_sync();
+                        const uint32_t vst = aK + s * kStageBytes;  // value dims are the window's first four boxes
 #pragma unroll
-                    for (int st = 0; st < kBlk / 16; ++st)
-                        tc::mma_bf16(tbase + kColO, tc::kmajor_desc(aP + 256u * st, kBlk),
-                                     tc::sw128_mnmajor_desc(vst + 2048u * st, kBoxBytes), idesc_o,
-                                     (ipv > 0 || st > 0) ? 1u : 0u);
-                    tc::mma_commit(&c.pv_done);
-                    tc::mma_commit(&c.empty[s]);
-                    ++ipv;
-                    progressed = true;
-                }
-                if (js < nblk && tc::mbar_ready(tc::smem_u32(&c.full[js % nst]), (uint32_t)(js / nst) & 1u) &&
-                    (js == 0 || tc::mbar_ready(tc::smem_u32(&c.s_empty), (uint32_t)(js - 1) & 1u))) {
-                    const int s = js % nst;
-                    tc::fence_after_sync();
-                    const uint32_t kst = aK + s * kStageBytes;
-#pragma unroll 2
-                    for (int st = 0; st < kQKHalf / 16; ++st) {
-                        const uint32_t e = 32u * h + 16u * st;  // window dim of this step (score dims start 32 in for h = 1)
-                        tc::mma_bf16_ta(tbase + kColS, tbase + kColQ + 8u * st,
-                                        tc::sw128_kmajor_desc(kst + (e >> 6) * kBoxBytes + (e & 63u) * 2u), idesc_s,
-                                        st > 0 ? 1u : 0u);
+                        for (int st = 0; st < kBlk / 16; ++st)
+                            tc::mma_bf16_ta(tbase + kColO, tbase + kColP + 8u * st,
+                                            tc::sw128_mnmajor_desc(vst + 2048u * st, kBoxBytes), idesc_o,
+                                            (ipv > 0 || st > 0) ? 1u : 0u);
+                        tc::mma_commit(&c.pv_done);
+                        tc::mma_commit(&c.empty[s]);
+                        ++ipv;
+                        progressed = true;
                     }
-                    tc::mma_commit(&c.s_full);
-                    ++js;
-                    progressed = true;
+                    if (js < nblk && tc::mbar_ready(tc::smem_u32(&c.full[js % nst]), (uint32_t)(js / nst) & 1u) &&
+                        (js == 0 || tc::mbar_ready(tc::smem_u32(&c.s_empty), (uint32_t)(js - 1) & 1u))) {
+                        const int s = js % nst;
+                        tc::fence_after_sync();
+                        const uint32_t kst = aK + s * kStageBytes;
+#pragma unroll 2
+                        for (int st = 0; st < kQKHalf / 16; ++st) {
+                            const uint32_t e = 32u * h + 16u * st;  // window dim of this step (score dims start 32 in for h = 1)
+                            tc::mma_bf16_ta(tbase + kColS, tbase + kColQ + 8u * st,
+                                            tc::sw128_kmajor_desc(kst + (e >> 6) * kBoxBytes + (e & 63u) * 2u), idesc_s,
+                                            st > 0 ? 1u : 0u);
+                        }
+                        tc::mma_commit(&c.s_full);
+                        ++js;
+                        progressed = true;
+                    }
+                    if (progressed) {
+                        idle = 0;
+                    } else if (++idle > kMaxPolls || ((idle & 255u) == 0 && *abort)) {
+                        ok = false;
+                    } else {
+                        __nanosleep(32);  // leave issue slots to the softmax warps on this sub-partition
+                    }
                 }
-                if (progressed) {
-                    idle = 0;
-                } else if (++idle > kMaxPolls || ((idle & 255u) == 0 && *abort)) {
-                    ok = false;
-                } else {
-                    __nanosleep(32);  // leave issue slots to the softmax warps on this sub-partition
-                }
+                if (!ok) give_up(c, &d.ctl[CTL_ERR]);
+                tc::mma_commit(&c.fin);
+                if (!tc::mbar_wait(&c.fin, 0, kMaxPolls)) give_up(c, &d.ctl[CTL_ERR]);
             }
-            if (!ok) give_up(c, &d.ctl[CTL_ERR]);
-            tc::mma_commit(&c.fin);
-            if (!tc::mbar_wait(&c.fin, 0, kMaxPolls)) give_up(c, &d.ctl[CTL_ERR]);
+            __syncwarp();
         }
-        __syncwarp();
     } else {
+        tc::regs_grow<kSoftmaxRegs>();
         // ---- softmax: two warpgroups; warp w serves heads 32(w%4) .. +31 (its tensor-memory lane
         // quarter) for keys [32 wg, 32 wg + 32) of every block, wg = w / 4 ----
         const int wg = warp >> 2;
@@ -447,8 +489,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
                 if (!(ok = produce(i + 1, cur))) break;
             }
             // mask of my 32 keys of the block (all real in the common case)
-            const int key = i * kBlk + kHalfBlk * wg + lane;
-            const uint32_t vm = __ballot_sync(0xFFFFFFFFu, key < k && sSl[key] >= 0);
+            const uint32_t vm = sMask[2 * i + wg];
             if (vm != 0xFFFFFFFFu) {
 #pragma unroll
                 for (int j = 0; j < kHalfBlk; ++j) sv[j] = (vm >> j) & 1u ? sv[j] : -INFINITY;
@@ -500,21 +541,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
                 for (int j = 0; j < kHalfBlk / 2; ++j) pk[j] = 0u;
             }
             l_run += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-            // the P tile is free once O += P(i-1) V(i-1) has completed
+            // P lives in tensor memory (A of O += P V); its columns are free once O += P(i-1) V(i-1)
+            // has completed
             if (i >= 1 && !(ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.pv_done, (uint32_t)(i - 1) & 1u, abort))))
                 break;
-#pragma unroll
-            for (int cc = 0; cc < kHalfBlk / 8; ++cc)
-                *reinterpret_cast<uint4*>(sP + tc::kmajor_chunk_offset(hd, 4 * wg + cc, kBlk)) =
-                    make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-            tc::fence_smem_async();
+            tc::fence_after_sync();
+            tc::tmem_st8_async(tl + kColP + (uint32_t)(kHalfBlk / 2 * wg), &pk[0]);
+            tc::tmem_st8_async(tl + kColP + (uint32_t)(kHalfBlk / 2 * wg) + 8u, &pk[8]);
+            tc::tmem_wait_st();
+            tc::fence_before_sync();
             tc::mbar_arrive(&c.p_full);
         }
         if (ok && nblk > 0) ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.pv_done, (uint32_t)(nblk - 1) & 1u, abort));
-        // the denominator is the two groups' shares summed in a fixed order (the same in both)
-        c.lpart[wg][hd] = l_run;
+        // the denominator is the two groups' shares summed in a fixed order (the same in both); the
+        // shares meet in the exchange tiles, idle once every softmax thread is past its last block
+        float* lpart = reinterpret_cast<float*>(sX);
         tc::named_sync(1, kSoftmaxThreads);  // every softmax thread gets here, aborted or not
-        const float l_all = c.lpart[0][hd] + c.lpart[1][hd];
+        lpart[wg * kHeads + hd] = l_run;
+        tc::named_sync(1, kSoftmaxThreads);
+        const float l_all = lpart[hd] + lpart[kHeads + hd];
         if (ok) {
             tc::fence_after_sync();
             uint16_t* o = out + ((size_t)uc * kHeads + hd) * 512 + h * kVHalf + kVHalf / 2 * wg;
@@ -545,10 +590,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
 
 }  // namespace
 
-size_t attend_smem_bytes(int k)
-{
-    return kOffK + (size_t)attend_stages(k) * kStageBytes + ((size_t)k * 4 + 15) / 16 * 16;
-}
+size_t attend_smem_bytes(int k) { return attend_layout(k).bytes; }
 
 // The hot buffer as a 2-D tensor of R*L*S rows by 576 bf16 (row stride 1152
 // bytes) for TMA: box one row by 64 columns, 128-byte swizzle, out-of-range
@@ -586,10 +628,11 @@ cudaError_t launch_attend(const void* hot_map, const Dev& d, const int32_t* req_
     static const cudaError_t attr = cudaFuncSetAttribute(attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                          (int)kSmemLimit);
     if (attr != cudaSuccess) return attr;
-    if (d.k > (int)kMaxTopk) return cudaErrorInvalidValue;
-    attend_kernel<<<call_units(d, B) * 2, kAttnThreads, attend_smem_bytes(d.k), st>>>(
+    const AttnLayout lay = attend_layout(d.k);
+    if (d.k > (int)kMaxTopk || lay.bytes > kSmemLimit) return cudaErrorInvalidValue;
+    attend_kernel<<<call_units(d, B) * 2, kAttnThreads, lay.bytes, st>>>(
         *static_cast<const CUtensorMap*>(hot_map), d, req_ids, static_cast<const uint16_t*>(q), slots,
-        static_cast<uint16_t*>(out), lse, sm_scale * 1.4426950408889634f, attend_stages(d.k));
+        static_cast<uint16_t*>(out), lse, sm_scale * 1.4426950408889634f, lay);
     return cudaGetLastError();
 }
 

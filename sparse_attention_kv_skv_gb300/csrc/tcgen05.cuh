@@ -286,6 +286,17 @@ __device__ __forceinline__ void named_sync(uint32_t id, uint32_t nthreads)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
+// Per-thread register budget of the executing warpgroup (all four warps execute it).
+template <int N>
+__device__ __forceinline__ void regs_grow()
+{
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_shrink()
+{
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
 // Every thread of both CTAs of the cluster.
 __device__ __forceinline__ void cluster_sync()
 {
