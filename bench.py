@@ -22,6 +22,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -109,7 +110,9 @@ class ClockSampler:
     def __init__(self, device: int, enabled: bool = True):
         self.device = device
         self.p = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        # raw samples go to a scratch file (SKV_BENCH_CLOCKS_DIR, else the temp directory)
+        out_dir = os.environ.get("SKV_BENCH_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(out_dir, f"skv_clocks_{os.getpid()}.csv")
         if enabled:
             try:
                 os.makedirs(os.path.dirname(self.path), exist_ok=True)
@@ -199,8 +202,8 @@ def hbm_peak_gbs():
 # dram__bytes_read.sum + dram__bytes_write.sum.  Valid only while the kernel
 # source is the one that was captured; scaled to other workloads by units.
 PROFILED_TRAFFIC = {"source": "sparse_attention_kv_skv_gb300/csrc/skv_step_kernels.cu",
-                    "sha256": "2dac0a375f4b917a2b98899aea467649508f7c79d30459126d9488e6b5cc0619",
-                    "units": 512, "dram_bytes": 42.669312e6 + 200.168192e6,
+                    "sha256": "8d62c9430bfe062f37f24aee3d4a0a50e36097b789fc6c89a43000a43cf221c6",
+                    "units": 512, "dram_bytes": 42.504192e6 + 197.452800e6,
                     "summary": "profiles/plan_gather_kernel_c2_16k_b64.md"}
 
 
