@@ -10,31 +10,33 @@
 // 576 dims; p = softmax over the keys; out = p . V with V the first 512 dims
 // of each key row; lse = log sum exp of the scaled scores.
 //
-// Kernel layout: a cluster of two CTAs per unit, keys in blocks of 64.  Tensor memory (512 columns
-// of 128 fp32 lanes) holds at most half of the 128 x 512 fp32 output, so CTA
-// h owns value dims [256h, 256h + 256) and, to split the score product too,
-// score dims [288h, 288h + 288): per block of 64 keys each CTA computes a
-// partial S over its 288 dims, the two partials are exchanged through
-// distributed shared memory (st.async, completing on the receiver's mbarrier)
-// and summed -- in the same fp32 addition on both sides, so both CTAs hold
-// bit-identical scores and run the same softmax.  Each CTA thus reads only a
-// 640-byte window of every key row (dims [256h, 256h + 320) cover both its
-// score and value dims) and no product is computed twice.
+// Kernel layout: a cluster of two CTAs per unit, keys in blocks of 64.
+// Tensor memory (512 columns of 128 fp32 lanes) holds at most half of the
+// 128 x 512 fp32 output, so CTA h owns value dims [256h, 256h + 256) and, to
+// split the score product too, score dims [288h, 288h + 288): per block each
+// CTA computes a partial S over its 288 dims for all 64 keys.  The scores are
+// then finished as a reduce-scatter through distributed shared memory: CTA h
+// keeps its partial of keys [32h, 32h + 32), sends the peer its partial of the
+// other 32 (st.async, completing on the peer's mbarrier), adds the peer's
+// partial of its own keys, and runs the softmax of those 32 keys; the two CTAs
+// swap their row maxima (so both take the same block maximum and keep the same
+// reference) and their halves of P, so each holds the whole P for O += P V over
+// its value half.  Each CTA reads only a 640-byte window of every key row
+// (dims [256h, 256h + 320) cover its score and value dims), and no product or
+// exponential is computed twice.
 //
-// Warp roles (192 threads): warps 0-3 the softmax warpgroup (thread t <->
-// head t <-> tensor-memory lane t: partial-score exchange, online softmax with
-// a lazily raised reference maximum -- the accumulator is rescaled only when
-// a block's maximum exceeds it by more than 2^8 --, P to shared memory,
-// epilogue); one thread of warp 4 issues the MMAs, in whichever of the two
-// streams (S of a later block, O += P V of the oldest) is ready first; one
-// thread of warp 5 gathers the key rows of each block into a ring of
-// shared-memory stages with TMA (tile::gather4: four rows by 64 dims per copy,
-// 128-byte swizzle; a masked slot is an out-of-range row, which reads zeros).
-// Q (this CTA's 288 score dims) sits in tensor memory as the A operand of
-// S = Q K^T, so shared-memory bandwidth goes to the keys alone; the swizzled
-// key stage is both the K-major B of S and, read as MN-major, the V of
-// O += P V.  Every wait is bounded: a timeout sets the sticky device error
-// bit and the CTA winds down.
+// Warp roles (512 threads): warpgroup 0 the softmax (thread t <-> head t <->
+// tensor-memory lane t; online softmax with a lazily raised reference maximum
+// -- the accumulator is rescaled only when a block's maximum exceeds it by
+// more than 2^8); warpgroup 1 sends the peer its partial scores; one thread of
+// warp 8 issues the MMAs, in whichever of the two streams (S of a later block,
+// O += P V of the oldest) is ready first; warps 9-15 gather the key rows of
+// each block into a ring of shared-memory stages with TMA (tile::gather4: four
+// rows by 64 dims per copy, 128-byte swizzle; a masked slot is an out-of-range
+// row, which reads zeros).  Q (this CTA's 288 score dims) sits in tensor memory
+// as the A operand of S = Q K^T; the swizzled key stage is both the K-major B
+// of S and, read as MN-major, the V of O += P V.  Every wait is bounded: a
+// timeout sets the sticky device error bit and the CTA winds down.
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -148,42 +150,45 @@ constexpr int kRowBytes = kDim * 2;
 constexpr int kVHalf = 256;      // value dims per CTA (of 512)
 constexpr int kQKHalf = kDim / 2;                        // score dims per CTA (288)
 constexpr int kBlk = 64;         // keys per block (the N of S = Q K^T)
-constexpr int kHalfBlk = kBlk / 2;                       // keys per softmax warpgroup
+constexpr int kHalfBlk = kBlk / 2;                       // keys of a block whose softmax this CTA finishes
 constexpr int kWinBoxes = 5;     // 64-dim column boxes of the key-row window a CTA loads (320 dims)
 constexpr int kMaxStages = 4;    // key stages in flight (3 when a long slot list needs the room)
-constexpr int kSoftmaxThreads = 256;                     // two warpgroups: keys [0, 32) and [32, 64) of a block
+constexpr int kSoftmaxThreads = 128;                     // warpgroup 0: one head a thread
+constexpr int kXchgWarp0 = 4;                            // warpgroup 1: sends the peer its partial scores
 constexpr int kMmaWarp = 8, kLoadWarp0 = 9, kLoadWarps = 7;
 constexpr int kAttnThreads = (kLoadWarp0 + kLoadWarps) * 32;  // 512 (128 registers a thread at launch)
-constexpr int kSoftmaxRegs = 168, kServiceRegs = 88;     // after the split (see the kernel)
-static_assert(kSoftmaxThreads * kSoftmaxRegs + (kAttnThreads - kSoftmaxThreads) * kServiceRegs ==
-                  kAttnThreads * (65536 / kAttnThreads),
-              "the register split must add up to the launch's registers");
+constexpr int kSoftmaxRegs = 192, kXchgRegs = 72, kServiceRegs = 88;  // after the split (see the kernel)
+static_assert(128 * (kSoftmaxRegs + kXchgRegs + 2 * kServiceRegs) <= 65536 &&
+                  32 * (kSoftmaxRegs + kXchgRegs + 2 * kServiceRegs) <= 16384,
+              "the register split must fit the launch's registers, also per SM sub-partition");
 constexpr int kGathers = kBlk / 4 * kWinBoxes;           // four-row TMA copies per block (80)
-constexpr uint32_t kXBytes = kHeads * kBlk * 4;          // one partial score tile (fp32): 32768
+constexpr uint32_t kXBytes = kHeads * kHalfBlk * 4;      // the peer's partial scores of my keys (fp32): 16384
+constexpr uint32_t kPBytes = kHeads * kBlk * 2;          // a P tile, both CTAs' halves (bf16): 16384
 constexpr uint32_t kBoxBytes = kBlk * 128;               // one column box of a key stage: 64 rows x 128 B
 constexpr uint32_t kStageBytes = kWinBoxes * kBoxBytes;  // 40960
 constexpr uint32_t kSmemLimit = 227 * 1024;              // dynamic shared memory a CTA may have (no static part)
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 0, kColS = 256, kColQ = 320, kColP = 464;  // O 256, S 64, Q 144, P 32 columns
+constexpr uint32_t kColO = 0, kColS = 256, kColQ = 320;  // O 256, S 64, Q 144 columns
 constexpr float kRescaleLog2 = 8.0f;                     // lazy rescale threshold (factor 256)
-static_assert(kColQ + kQKHalf / 2 <= kColP && kColP + kBlk / 2 <= kTmemCols && kColS + kBlk <= kColQ,
-              "tensor-memory columns");
+static_assert(kColQ + kQKHalf / 2 <= kTmemCols && kColS + kBlk <= kColQ, "tensor-memory columns");
 
 struct alignas(16) AttnCtl;
 // Shared-memory layout for a slot list of k entries: the key stages first
-// (1024-byte aligned for the swizzle), then the two exchange tiles, the
-// per-block masks of real keys (two words a block) and the control block.
+// (1024-byte aligned for the swizzle), then the two exchange tiles, the two
+// P tiles, the per-block masks of real keys (two words a block) and the
+// control block.
 struct AttnLayout {
     int stages;
-    uint32_t off_x, off_mask, off_ctl, bytes;
+    uint32_t off_x, off_p, off_mask, off_ctl, bytes;
 };
 __host__ __device__ constexpr uint32_t attend_ctl_bytes();
 __host__ __device__ inline AttnLayout attend_layout(int k)
 {
     const uint32_t masks = (uint32_t)((k + kBlk - 1) / kBlk) * 8u;
     for (int st = kMaxStages;; --st) {
-        AttnLayout a{st, (uint32_t)st * kStageBytes, 0, 0, 0};
-        a.off_mask = a.off_x + 2 * kXBytes;
+        AttnLayout a{st, (uint32_t)st * kStageBytes, 0, 0, 0, 0};
+        a.off_p = a.off_x + 2 * kXBytes;
+        a.off_mask = a.off_p + 2 * kPBytes;
         a.off_ctl = (a.off_mask + masks + 15u) & ~15u;
         a.bytes = a.off_ctl + attend_ctl_bytes();
         if (a.bytes <= kSmemLimit || st == 2) return a;
@@ -210,14 +215,17 @@ struct alignas(16) AttnCtl {
     uint64_t full[kMaxStages];   // key stage landed (TMA transaction bytes; one arrive per loader)
     uint64_t empty[kMaxStages];  // key stage consumed by its last product
     uint64_t s_full;             // partial S of the next block is in tensor memory
-    uint64_t s_empty;            // the softmax warpgroups have read it
-    uint64_t x_full[2];          // the peer's partial S of a block has arrived (32768 transaction bytes)
-    uint64_t m_full[2];          // both warpgroups' partial row maxima of a block are in `mpart`
-    uint64_t p_full;             // P of the block is in tensor memory
-    uint64_t pv_done;            // O += P V of the block has completed
+    uint64_t s_empty;            // the softmax and exchange warpgroups have read it
+    uint64_t adv;                // the softmax warpgroup has taken a block's row maxima (one phase a block)
+    uint64_t x_full[2];          // the peer's partial scores of my keys of a block have arrived (16384 bytes)
+    uint64_t m_full[2];          // the peer's row maxima of a block have arrived (512 bytes)
+    uint64_t p_full[2];          // a P tile is complete: my half written, the peer's half arrived (8192 bytes)
+    uint64_t pv_done[2];         // O += P V of a block has completed
+    uint64_t l_full;             // the peer's share of the softmax denominators has arrived (512 bytes)
     uint64_t q_ready;            // Q is in tensor memory
     uint64_t fin;                // every MMA this CTA issued has completed
-    float mpart[2][2][kHeads];   // [block parity][warpgroup][head] partial row maxima of the raw scores
+    float mx[2][kHeads];         // [block parity][head] the peer's row maxima of the raw scores
+    float lx[kHeads];            // [head] the peer's share of the denominator
     uint32_t tmem_base;
     uint32_t abort;              // a wait of this CTA gave up
 };
@@ -277,6 +285,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
     const int nblk = (k + kBlk - 1) / kBlk;
     uint8_t* sK = smem;  // key stages
     uint8_t* sX = smem + lay.off_x;
+    uint8_t* sP = smem + lay.off_p;
     uint32_t* sMask = reinterpret_cast<uint32_t*>(smem + lay.off_mask);  // bit j of word 2i + g: key 64i + 32g + j is real
     volatile uint32_t* abort = &c.abort;
 
@@ -292,13 +301,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
             tc::mbar_init(&c.empty[s], 1);
         }
         tc::mbar_init(&c.s_full, 1);
-        tc::mbar_init(&c.s_empty, kSoftmaxThreads);
+        tc::mbar_init(&c.s_empty, 2 * kSoftmaxThreads);  // the softmax and the exchange warpgroups
+        tc::mbar_init(&c.adv, kSoftmaxThreads);
         for (int i = 0; i < 2; ++i) {
-            tc::mbar_init(&c.x_full[i], 1);
-            tc::mbar_init(&c.m_full[i], kSoftmaxThreads);
+            tc::mbar_init(&c.x_full[i], 1);                // one expect_tx arrival + the peer's bytes
+            tc::mbar_init(&c.m_full[i], 1);
+            tc::mbar_init(&c.p_full[i], kSoftmaxThreads);  // my half (one of them with expect_tx) + the peer's bytes
+            tc::mbar_init(&c.pv_done[i], 1);
         }
-        tc::mbar_init(&c.p_full, kSoftmaxThreads);
-        tc::mbar_init(&c.pv_done, 1);
+        tc::mbar_init(&c.l_full, 1);
         tc::mbar_init(&c.q_ready, kSoftmaxThreads);
         tc::mbar_init(&c.fin, 1);
         c.abort = 0u;
@@ -308,10 +319,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
     tc::cluster_sync();  // barriers of both CTAs exist before either sends to the other; masks staged
     tc::fence_after_sync();
     const uint32_t tbase = c.tmem_base;
-    // Register split (warpgroup-wide): the two softmax warpgroups take 168 a thread, the MMA and
-    // loader warpgroups give theirs down to 88 -- 256 x 168 + 256 x 88 = 512 x 128, the launch's
-    // total, and per SM sub-partition 2 x 168 + 2 x 88 = 4 x 128 as well.
-
+    // Register split (warpgroup-wide): softmax 192 a thread, exchange 72, MMA and loaders 88; the
+    // shares fit the launch's 512 x 128 in total and on every SM sub-partition (one warp of each
+    // warpgroup per sub-partition).
     if (warp >= kMmaWarp) {
         tc::regs_shrink<kServiceRegs>();
         if (warp >= kLoadWarp0) {
@@ -329,6 +339,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
                 return slot >= 0 && slot < S ? slot : -1;
             };
             int32_t v0 = fetch(0, 0), v1 = fetch(0, 1);
+            // loader 0 also warms L2 with the rows of block i + nst while block i is issued: when that
+            // block's stage frees up, its copies then come from L2 (the stage's life is the pipeline's
+            // limit); the slots of the block to warm are fetched one block ahead
+            const uint8_t* win = d.hot + (size_t)row0 * kRowBytes + 512u * h;  // this CTA's window of row 0
+            int32_t w0 = lw == 0 && nst < nblk ? fetch(nst, 0) : -1, w1 = lw == 0 && nst < nblk ? fetch(nst, 1) : -1;
             int last[kMaxStages] = {-1, -1, -1, -1};  // last block issued into each stage
             bool ok = true;
             for (int i = 0; i < nblk; ++i) {
@@ -353,6 +368,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
                         tc::tma_gather4(tc::smem_u32(sK + s * kStageBytes) + cb * kBoxBytes + g * 512u, &hot_map,
                                         256 * (int)h + 64 * cb, rr[0], rr[1], rr[2], rr[3], &c.full[s]);
                 }
+                if (lw == 0 && i + nst < nblk) {
+#pragma unroll
+                    for (int cb = 0; cb < kWinBoxes; ++cb) {
+                        if (w0 >= 0) tc::prefetch_l2(win + (size_t)w0 * kRowBytes + 128 * cb);
+                        if (w1 >= 0) tc::prefetch_l2(win + (size_t)w1 * kRowBytes + 128 * cb);
+                    }
+                    const bool more = i + nst + 1 < nblk;
+                    w0 = more ? fetch(i + nst + 1, 0) : -1;
+                    w1 = more ? fetch(i + nst + 1, 1) : -1;
+                }
                 last[s] = i;
                 v0 = n0;
                 v1 = n1;
@@ -366,28 +391,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
             __syncwarp();
         } else {
             // ---- MMA issuer: whichever product is ready first.  O += P(i) V(i) as soon as P(i) is
-            // written (it frees the key stage for the loaders); S(j) as soon as its keys have landed
+            // complete (it frees the key stage for the loaders); S(j) as soon as its keys have landed
             // and S(j-1) has been read out of tensor memory.  Both streams are issued in order. ----
             if (lane == 0) {
                 const uint32_t idesc_s = tc::idesc_bf16_f32(kHeads, kBlk, 0);
                 const uint32_t idesc_o = tc::idesc_bf16_f32(kHeads, kVHalf, 1);
-                const uint32_t aK = tc::smem_u32(sK);
+                const uint32_t aK = tc::smem_u32(sK), aP = tc::smem_u32(sP);
                 bool ok = wait_phase(&c.q_ready, 0, abort);
                 tc::fence_after_sync();
                 int js = 0, ipv = 0;  // next S block, next P V block
                 uint32_t idle = 0;
                 while (ok && ipv < nblk) {
                     bool progressed = false;
-                    if (ipv < js && tc::mbar_ready(tc::smem_u32(&c.p_full), (uint32_t)ipv & 1u)) {
-                        const int s = ipv % nst;
+                    if (ipv < js && tc::mbar_ready(tc::smem_u32(&c.p_full[ipv & 1]), (uint32_t)(ipv >> 1) & 1u)) {
+                        const int bb = ipv & 1, s = ipv % nst;
+                        tc::fence_smem_async();  // the peer's half arrived through the generic proxy
                         tc::fence_after_sync();
                         const uint32_t vst = aK + s * kStageBytes;  // value dims are the window's first four boxes
 #pragma unroll
                         for (int st = 0; st < kBlk / 16; ++st)
-                            tc::mma_bf16_ta(tbase + kColO, tbase + kColP + 8u * st,
-                                            tc::sw128_mnmajor_desc(vst + 2048u * st, kBoxBytes), idesc_o,
-                                            (ipv > 0 || st > 0) ? 1u : 0u);
-                        tc::mma_commit(&c.pv_done);
+                            tc::mma_bf16(tbase + kColO, tc::kmajor_desc(aP + bb * kPBytes + 256u * st, kBlk),
+                                         tc::sw128_mnmajor_desc(vst + 2048u * st, kBoxBytes), idesc_o,
+                                         (ipv > 0 || st > 0) ? 1u : 0u);
+                        tc::mma_commit(&c.pv_done[bb]);
                         tc::mma_commit(&c.empty[s]);
                         ++ipv;
                         progressed = true;
@@ -401,8 +427,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
                         for (int st = 0; st < kQKHalf / 16; ++st) {
                             const uint32_t e = 32u * h + 16u * st;  // window dim of this step (score dims start 32 in for h = 1)
                             tc::mma_bf16_ta(tbase + kColS, tbase + kColQ + 8u * st,
-                                            tc::sw128_kmajor_desc(kst + (e >> 6) * kBoxBytes + (e & 63u) * 2u), idesc_s,
-                                            st > 0 ? 1u : 0u);
+                                            tc::sw128_kmajor_desc(kst + (e >> 6) * kBoxBytes + (e & 63u) * 2u),
+                                            idesc_s, st > 0 ? 1u : 0u);
                         }
                         tc::mma_commit(&c.s_full);
                         ++js;
@@ -413,7 +439,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
                     } else if (++idle > kMaxPolls || ((idle & 255u) == 0 && *abort)) {
                         ok = false;
                     } else {
-                        __nanosleep(32);  // leave issue slots to the softmax warps on this sub-partition
+                        __nanosleep(32);  // leave issue slots to the warps on this sub-partition
                     }
                 }
                 if (!ok) give_up(c, &d.ctl[CTL_ERR]);
@@ -422,17 +448,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
             }
             __syncwarp();
         }
-    } else {
-        tc::regs_grow<kSoftmaxRegs>();
-        // ---- softmax: two warpgroups; warp w serves heads 32(w%4) .. +31 (its tensor-memory lane
-        // quarter) for keys [32 wg, 32 wg + 32) of every block, wg = w / 4 ----
-        const int wg = warp >> 2;
-        const int hd = ((warp & 3) << 5) | lane;  // head = tensor-memory lane
+    } else if (warp >= kXchgWarp0) {
+        // ---- exchange warpgroup: thread t <-> head t.  For every block, the peer's 32 keys of my
+        // partial S go straight from tensor memory into the peer's exchange tile (st.async; the bytes
+        // complete on the peer's x_full).  Block j is sent only once my softmax has taken block
+        // j - 2's maxima -- which it cannot do before the peer has read block j - 2's tile, the
+        // previous user of the buffer. ----
+        tc::regs_shrink<kXchgRegs>();
+        const int hd = tid - kSoftmaxThreads;
         const uint32_t tl = tbase + ((uint32_t)((warp & 3) * 32) << 16);
-        {   // Q: this head's 288 score dims into columns [kColQ, kColQ + 144); groups of 16 columns,
-            // warpgroup 0 the first five, warpgroup 1 the other four
+        const uint32_t x_peer = tc::map_to_rank(tc::smem_u32(sX), peer) + (uint32_t)hd * 16u;
+        const uint32_t xf0 = tc::map_to_rank(tc::smem_u32(&c.x_full[0]), peer);
+        const uint32_t xf1 = tc::map_to_rank(tc::smem_u32(&c.x_full[1]), peer);
+        bool ok = true;
+        for (int j = 0; ok && j < nblk; ++j) {
+            if (j >= 2 && !(ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.adv, (uint32_t)(j - 2) & 1u, abort)))) break;
+            if (!(ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.s_full, (uint32_t)j & 1u, abort)))) break;
+            tc::fence_after_sync();
+            float v[kHalfBlk];
+            tc::tmem_ld32(tl + kColS + (uint32_t)(kHalfBlk * peer), v);
+            tc::fence_before_sync();
+            tc::mbar_arrive(&c.s_empty);
+            const uint32_t xb = x_peer + (uint32_t)(j & 1) * kXBytes;
+            const uint32_t rb = (j & 1) ? xf1 : xf0;
+#pragma unroll
+            for (int m = 0; m < kHalfBlk / 4; ++m)
+                tc::st_async16(xb + 2048u * m, v[4 * m], v[4 * m + 1], v[4 * m + 2], v[4 * m + 3], rb);
+        }
+        if (!ok) give_up(c, &d.ctl[CTL_ERR]);
+    } else {
+        // ---- softmax warpgroup: thread t <-> head t <-> tensor-memory lane t, my 32 keys of every
+        // block (keys [32h, 32h + 32)); both CTAs take the same block maxima, so they keep the same
+        // reference and their P halves fit one P V product ----
+        tc::regs_grow<kSoftmaxRegs>();
+        const int hd = tid;
+        const uint32_t tl = tbase + ((uint32_t)(warp * 32) << 16);
+        {   // Q: this head's 288 score dims into columns [kColQ, kColQ + 144)
             const uint4* qr = reinterpret_cast<const uint4*>(q + ((size_t)uc * kHeads + hd) * kDim + h * kQKHalf);
-            for (int g = wg * 5; g < (wg ? kQKHalf / 32 : 5); ++g) {
+#pragma unroll 3
+            for (int g = 0; g < kQKHalf / 32; ++g) {  // 9 groups of 16 columns
                 uint4 a = qr[4 * g], bq = qr[4 * g + 1], cq4 = qr[4 * g + 2], dq = qr[4 * g + 3];
                 const uint32_t w0[8] = {a.x, a.y, a.z, a.w, bq.x, bq.y, bq.z, bq.w};
                 const uint32_t w1[8] = {cq4.x, cq4.y, cq4.z, cq4.w, dq.x, dq.y, dq.z, dq.w};
@@ -443,39 +497,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
             tc::fence_before_sync();
             tc::mbar_arrive(&c.q_ready);
         }
-        // Partial scores are exchanged one block ahead: this CTA's partial of
-        // block j is stored straight from registers into the peer's buffer
-        // j % 2 (st.async; the bytes complete on the peer's x_full[j % 2]).
-        // Block j + 1 is sent only after the peer's block j has arrived here,
-        // which the peer sends after it has read block j - 1 -- the previous
-        // user of that buffer.  Layout: [16-byte group m of 4 keys][head].
-        const uint32_t x_peer = tc::map_to_rank(tc::smem_u32(sX), peer) + (uint32_t)hd * 16u + (uint32_t)wg * 8u * 2048u;
-        const uint32_t xf0 = tc::map_to_rank(tc::smem_u32(&c.x_full[0]), peer);
-        const uint32_t xf1 = tc::map_to_rank(tc::smem_u32(&c.x_full[1]), peer);
-        // this CTA's partial S of block j, my 32 keys: tensor memory -> registers -> the peer
-        auto produce = [&](int j, float (&dst)[kHalfBlk]) -> bool {
+        const uint32_t mx_peer = tc::map_to_rank(tc::smem_u32(&c.mx[0][0]), peer) + (uint32_t)hd * 4u;
+        const uint32_t mf0 = tc::map_to_rank(tc::smem_u32(&c.m_full[0]), peer);
+        const uint32_t mf1 = tc::map_to_rank(tc::smem_u32(&c.m_full[1]), peer);
+        const uint32_t p_peer = tc::map_to_rank(tc::smem_u32(sP), peer);
+        const uint32_t pf0 = tc::map_to_rank(tc::smem_u32(&c.p_full[0]), peer);
+        const uint32_t pf1 = tc::map_to_rank(tc::smem_u32(&c.p_full[1]), peer);
+        auto own = [&](int j, float (&dst)[kHalfBlk]) -> bool {  // my keys of my partial S(j)
             if (!__all_sync(0xFFFFFFFFu, wait_phase(&c.s_full, (uint32_t)j & 1u, abort))) return false;
             tc::fence_after_sync();
-            tc::tmem_ld32(tl + kColS + (uint32_t)(kHalfBlk * wg), dst);
+            tc::tmem_ld32(tl + kColS + (uint32_t)(kHalfBlk * h), dst);
             tc::fence_before_sync();
             tc::mbar_arrive(&c.s_empty);
-            const uint32_t xb = x_peer + (uint32_t)(j & 1) * kXBytes;
-            const uint32_t rb = (j & 1) ? xf1 : xf0;
-#pragma unroll
-            for (int m = 0; m < kHalfBlk / 4; ++m)
-                tc::st_async16(xb + 2048u * m, dst[4 * m], dst[4 * m + 1], dst[4 * m + 2], dst[4 * m + 3], rb);
             return true;
         };
-        float m_ref = -INFINITY;  // reference maximum (log2 domain) the exponentials use; equal in both groups
-        float l_run = 0.0f;       // this group's share of the softmax denominator
-        float cur[kHalfBlk];      // this CTA's partial S of the block being processed (my keys)
+        float m_ref = -INFINITY;  // reference maximum (log2 domain) the exponentials use; equal in both CTAs
+        float l_run = 0.0f;       // this CTA's share of the softmax denominator
+        float cur[kHalfBlk];      // my partial S of the block being processed, my keys
         if (tid == 0) tc::mbar_arrive_expect_tx(&c.x_full[0], kXBytes);
-        bool ok = produce(0, cur);
+        bool ok = own(0, cur);
         for (int i = 0; ok && i < nblk; ++i) {
             const int bb = i & 1;
-            if (!(ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.x_full[bb], (uint32_t)(i >> 1) & 1u, abort)))) break;
-            float sv[kHalfBlk];  // own + peer: the same fp32 sum on both CTAs
-            const uint8_t* xrow = sX + bb * kXBytes + wg * 8 * 2048 + hd * 16;
+            const uint32_t ph = (uint32_t)(i >> 1) & 1u;
+            if (!(ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.x_full[bb], ph, abort)))) break;
+            float sv[kHalfBlk];  // mine + the peer's partial: the full scores of my keys
+            const uint8_t* xrow = sX + bb * kXBytes + hd * 16;
 #pragma unroll
             for (int m = 0; m < kHalfBlk / 4; ++m) {
                 const float4 pr = *reinterpret_cast<const float4*>(xrow + 2048 * m);
@@ -484,37 +530,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
                 sv[4 * m + 2] = cur[4 * m + 2] + pr.z;
                 sv[4 * m + 3] = cur[4 * m + 3] + pr.w;
             }
-            if (i + 1 < nblk) {  // block i + 1 travels while this block's softmax runs
+            if (i + 1 < nblk) {
                 if (tid == 0) tc::mbar_arrive_expect_tx(&c.x_full[bb ^ 1], kXBytes);
-                if (!(ok = produce(i + 1, cur))) break;
+                if (!(ok = own(i + 1, cur))) break;
             }
-            // mask of my 32 keys of the block (all real in the common case)
-            const uint32_t vm = sMask[2 * i + wg];
+            const uint32_t vm = sMask[2 * i + h];
             if (vm != 0xFFFFFFFFu) {
 #pragma unroll
                 for (int j = 0; j < kHalfBlk; ++j) sv[j] = (vm >> j) & 1u ? sv[j] : -INFINITY;
             }
-            // row maximum of the raw scores over the block (scale > 0 keeps the order):
-            // a tree over my 32 keys, then the other group's half through shared memory
             float mx[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j)
                 mx[j] = fmaxf(fmaxf(fmaxf(sv[j], sv[j + 4]), fmaxf(sv[j + 8], sv[j + 12])),
                               fmaxf(fmaxf(sv[j + 16], sv[j + 20]), fmaxf(sv[j + 24], sv[j + 28])));
-            c.mpart[bb][wg][hd] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-            tc::mbar_arrive(&c.m_full[bb]);
-            if (!(ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.m_full[bb], (uint32_t)(i >> 1) & 1u, abort)))) break;
-            const float mb = fmaxf(c.mpart[bb][0][hd], c.mpart[bb][1][hd]) * scale_log2;
+            const float mloc = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+            // P tile bb (mine and, once I send my maxima, the peer's half) is free once O += P(i-2) V(i-2)
+            // has completed; the peer sends its P(i) only after my maxima of block i
+            if (i >= 2 && !(ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.pv_done[bb], ((i - 2) >> 1) & 1, abort))))
+                break;
+            if (tid == 0) tc::mbar_arrive_expect_tx(&c.m_full[bb], kHeads * 4u);
+            tc::st_async4(mx_peer + (uint32_t)bb * kHeads * 4u, mloc, bb ? mf1 : mf0);
+            if (!(ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.m_full[bb], ph, abort)))) break;
+            const float mb = fmaxf(mloc, c.mx[bb][hd]) * scale_log2;  // the same in both CTAs
+            tc::mbar_arrive(&c.adv);  // the exchange warpgroup may now send block i + 2
             float factor = 1.0f;
             if (mb > m_ref + kRescaleLog2) {
                 factor = m_ref == -INFINITY ? 0.0f : ex2(m_ref - mb);
                 m_ref = mb;
                 l_run *= factor;
             }
-            if (i > 0 && __any_sync(0xFFFFFFFFu, factor != 1.0f)) {  // rescale my half of this warp's rows of O
-                if (!(ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.pv_done, (uint32_t)(i - 1) & 1u, abort)))) break;
+            if (i > 0 && __any_sync(0xFFFFFFFFu, factor != 1.0f)) {  // rescale this warp's rows of O
+                if (!(ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, abort))))
+                    break;
                 tc::fence_after_sync();
-                for (int c0 = kVHalf / 2 * wg; c0 < kVHalf / 2 * (wg + 1); c0 += 32) {
+                for (int c0 = 0; c0 < kVHalf; c0 += 32) {
                     float ov[32];
                     tc::tmem_ld32(tl + kColO + c0, ov);
 #pragma unroll
@@ -541,39 +591,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
                 for (int j = 0; j < kHalfBlk / 2; ++j) pk[j] = 0u;
             }
             l_run += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-            // P lives in tensor memory (A of O += P V); its columns are free once O += P(i-1) V(i-1)
-            // has completed
-            if (i >= 1 && !(ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.pv_done, (uint32_t)(i - 1) & 1u, abort))))
-                break;
-            tc::fence_after_sync();
-            tc::tmem_st8_async(tl + kColP + (uint32_t)(kHalfBlk / 2 * wg), &pk[0]);
-            tc::tmem_st8_async(tl + kColP + (uint32_t)(kHalfBlk / 2 * wg) + 8u, &pk[8]);
-            tc::tmem_wait_st();
-            tc::fence_before_sync();
-            tc::mbar_arrive(&c.p_full);
+            // my half of P(i): into my tile and into the peer's, at the same place (keys [32h, 32h + 32))
+            const uint32_t pb = (uint32_t)bb * kPBytes;
+#pragma unroll
+            for (int cc = 0; cc < kHalfBlk / 8; ++cc) {
+                const uint32_t off = pb + tc::kmajor_chunk_offset(hd, 4 * h + cc, kBlk);
+                const uint4 w4 = make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+                *reinterpret_cast<uint4*>(sP + off) = w4;
+                tc::st_async16u(p_peer + off, w4, bb ? pf1 : pf0);
+            }
+            tc::fence_smem_async();
+            if (tid == 0)
+                tc::mbar_arrive_expect_tx(&c.p_full[bb], kPBytes / 2);  // my arrival + the peer's half
+            else
+                tc::mbar_arrive(&c.p_full[bb]);
         }
-        if (ok && nblk > 0) ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.pv_done, (uint32_t)(nblk - 1) & 1u, abort));
-        // the denominator is the two groups' shares summed in a fixed order (the same in both); the
-        // shares meet in the exchange tiles, idle once every softmax thread is past its last block
-        float* lpart = reinterpret_cast<float*>(sX);
-        tc::named_sync(1, kSoftmaxThreads);  // every softmax thread gets here, aborted or not
-        lpart[wg * kHeads + hd] = l_run;
-        tc::named_sync(1, kSoftmaxThreads);
-        const float l_all = lpart[hd] + lpart[kHeads + hd];
+        if (ok && nblk > 0) ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.pv_done[(nblk - 1) & 1], ((nblk - 1) >> 1) & 1, abort));
+        // the denominator: CTA 0's share + CTA 1's share, in that order on both CTAs
+        if (tid == 0) tc::mbar_arrive_expect_tx(&c.l_full, kHeads * 4u);
+        tc::st_async4(tc::map_to_rank(tc::smem_u32(&c.lx[0]), peer) + (uint32_t)hd * 4u, l_run,
+                      tc::map_to_rank(tc::smem_u32(&c.l_full), peer));
+        if (ok) ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.l_full, 0u, abort));
         if (ok) {
+            const float l_all = h == 0 ? l_run + c.lx[hd] : c.lx[hd] + l_run;
             tc::fence_after_sync();
-            uint16_t* o = out + ((size_t)uc * kHeads + hd) * 512 + h * kVHalf + kVHalf / 2 * wg;
+            uint16_t* o = out + ((size_t)uc * kHeads + hd) * 512 + h * kVHalf;
             const float inv = l_all > 0.0f ? 1.0f / l_all : 0.0f;
-            for (int c0 = 0; c0 < kVHalf / 2; c0 += 32) {
+            for (int c0 = 0; c0 < kVHalf; c0 += 32) {
                 float ov[32];
-                tc::tmem_ld32(tl + kColO + kVHalf / 2 * wg + c0, ov);
+                tc::tmem_ld32(tl + kColO + c0, ov);
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc)
                     *reinterpret_cast<uint4*>(o + c0 + 8 * cc) =
                         make_uint4(bf2(ov[8 * cc] * inv, ov[8 * cc + 1] * inv), bf2(ov[8 * cc + 2] * inv, ov[8 * cc + 3] * inv),
                                    bf2(ov[8 * cc + 4] * inv, ov[8 * cc + 5] * inv), bf2(ov[8 * cc + 6] * inv, ov[8 * cc + 7] * inv));
             }
-            if (h == 0 && wg == 0 && lse)
+            if (h == 0 && lse)
                 lse[(size_t)uc * kHeads + hd] = l_all > 0.0f ? (m_ref + log2f(l_all)) * 0.69314718055994531f : -INFINITY;
         } else {
             give_up(c, &d.ctl[CTL_ERR]);

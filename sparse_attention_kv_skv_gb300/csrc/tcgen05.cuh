@@ -262,6 +262,24 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const void* map, int x
         : "memory");
 }
 
+// The same for 4 bytes, and for 16 bytes given as a uint4.
+__device__ __forceinline__ void st_async4(uint32_t remote_addr, float a, uint32_t remote_bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(remote_addr),
+                 "r"(__float_as_uint(a)), "r"(remote_bar)
+                 : "memory");
+}
+__device__ __forceinline__ void st_async16u(uint32_t remote_addr, uint4 v, uint32_t remote_bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     remote_addr),
+                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(remote_bar)
+                 : "memory");
+}
+
+// Bring the 128-byte line at `p` (global memory) into L2.
+__device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
+
 // Shared-memory address of the same variable in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank)
 {

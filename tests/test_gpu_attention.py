@@ -124,3 +124,33 @@ def test_attention_short_topk_and_non_request(k):
         assert p.ctx.get_device_error() == 0
     finally:
         p.close()
+
+
+@pytest.mark.fullsize
+def test_attention_full_size_sampled():
+    """The bench's launch configuration: the 192 x 8 target workload (k = 2048,
+    S = 4096) after a cold and two steady steps, one call over all 1536 units;
+    a spread of units is checked against the definition on the oracle's hot
+    buffer."""
+    w = wl.WORKLOADS["target_16k_b192_f20"]
+    p = Pair(w)
+    try:
+        for s in range(3):
+            p.step(s)
+        units = [(b, l) for b in range(w.B) for l in range(w.L)]
+        q = _queries(w, units)
+        out_d = torch.full((len(units), 128, 512), 0x7FC0, dtype=torch.int16, device="cuda")
+        lse_d = torch.full((len(units), 128), float("nan"), device="cuda")
+        scale = 1.0 / 576 ** 0.5
+        p.ctx.attend(p.req_dev, torch.from_numpy(q).cuda(), p.slots_dev, out_d, lse_d, sm_scale=scale)
+        torch.cuda.synchronize()
+        assert p.ctx.get_device_error() == 0
+        pick = [n for n, (b, l) in enumerate(units)
+                if (b, l) in {(0, 0), (0, 7), (1, 3), (63, 5), (95, 4), (127, 1), (190, 6), (191, 7)}]
+        slots = p.slots_dev.cpu().numpy().reshape(len(units), w.k)[pick]
+        out = out_d.cpu().numpy().view(np.uint16)[pick]
+        lse = lse_d.cpu().numpy()[pick]
+        _check_units(p, [units[n] for n in pick], slots, q[pick], out, lse, scale)
+        assert np.isfinite(lse_d.cpu().numpy()).all()  # every unit of the call produced a result
+    finally:
+        p.close()
