@@ -10,7 +10,10 @@
 // 576 dims; p = softmax over the keys; out = p . V with V the first 512 dims
 // of each key row; lse = log sum exp of the scaled scores.
 //
-// Kernel layout: a cluster of two CTAs per unit, keys in blocks of 64.
+// Kernel layout: persistent clusters of two CTAs (one CTA per SM), each
+// cluster walking its share of the units in turn, keys in blocks of 64; blocks
+// are numbered across a cluster's units, so the key pipeline and every
+// exchange run on from one unit into the next.
 // Tensor memory (512 columns of 128 fp32 lanes) holds at most half of the
 // 128 x 512 fp32 output, so CTA h owns value dims [256h, 256h + 256) and, to
 // split the score product too, score dims [288h, 288h + 288): per block each
@@ -41,6 +44,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cmath>
 #include <string>
 
@@ -173,23 +177,20 @@ constexpr float kRescaleLog2 = 8.0f;                     // lazy rescale thresho
 static_assert(kColQ + kQKHalf / 2 <= kTmemCols && kColS + kBlk <= kColQ, "tensor-memory columns");
 
 struct alignas(16) AttnCtl;
-// Shared-memory layout for a slot list of k entries: the key stages first
-// (1024-byte aligned for the swizzle), then the two exchange tiles, the two
-// P tiles, the per-block masks of real keys (two words a block) and the
-// control block.
+// Shared-memory layout: the key stages first (1024-byte aligned for the
+// swizzle), then the two exchange tiles, the two P tiles and the control
+// block.
 struct AttnLayout {
     int stages;
-    uint32_t off_x, off_p, off_mask, off_ctl, bytes;
+    uint32_t off_x, off_p, off_ctl, bytes;
 };
 __host__ __device__ constexpr uint32_t attend_ctl_bytes();
-__host__ __device__ inline AttnLayout attend_layout(int k)
+__host__ __device__ inline AttnLayout attend_layout()
 {
-    const uint32_t masks = (uint32_t)((k + kBlk - 1) / kBlk) * 8u;
     for (int st = kMaxStages;; --st) {
-        AttnLayout a{st, (uint32_t)st * kStageBytes, 0, 0, 0, 0};
+        AttnLayout a{st, (uint32_t)st * kStageBytes, 0, 0, 0};
         a.off_p = a.off_x + 2 * kXBytes;
-        a.off_mask = a.off_p + 2 * kPBytes;
-        a.off_ctl = (a.off_mask + masks + 15u) & ~15u;
+        a.off_ctl = a.off_p + 2 * kPBytes;
         a.bytes = a.off_ctl + attend_ctl_bytes();
         if (a.bytes <= kSmemLimit || st == 2) return a;
     }
@@ -221,8 +222,9 @@ struct alignas(16) AttnCtl {
     uint64_t m_full[2];          // the peer's row maxima of a block have arrived (512 bytes)
     uint64_t p_full[2];          // a P tile is complete: my half written, the peer's half arrived (8192 bytes)
     uint64_t pv_done[2];         // O += P V of a block has completed
-    uint64_t l_full;             // the peer's share of the softmax denominators has arrived (512 bytes)
-    uint64_t q_ready;            // Q is in tensor memory
+    uint64_t l_full;             // the peer's share of the softmax denominators has arrived (512 bytes; a phase a unit)
+    uint64_t q_ready;            // a unit's Q is in tensor memory (a phase a unit)
+    uint64_t o_free;             // the softmax has read a unit's accumulator out of tensor memory (a phase a unit)
     uint64_t fin;                // every MMA this CTA issued has completed
     float mx[2][kHeads];         // [block parity][head] the peer's row maxima of the raw scores
     float lx[kHeads];            // [head] the peer's share of the denominator
@@ -257,44 +259,38 @@ __device__ __forceinline__ void give_up(AttnCtl& c, uint32_t* err)
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
     attend_kernel(const __grid_constant__ CUtensorMap hot_map, Dev d, const int32_t* __restrict__ req_ids,
                   const uint16_t* __restrict__ q, const int32_t* __restrict__ slots, uint16_t* __restrict__ out,
-                  float* __restrict__ lse, float scale_log2, AttnLayout lay)
+                  float* __restrict__ lse, float scale_log2, AttnLayout lay, int units)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
     AttnCtl& c = *reinterpret_cast<AttnCtl*>(smem + lay.off_ctl);
     const int nst = lay.stages;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int uc = blockIdx.x >> 1;                        // unit of the call
+    const int cl = blockIdx.x >> 1, ncl = gridDim.x >> 1;  // this cluster; clusters of the grid
     const uint32_t h = blockIdx.x & 1u, peer = h ^ 1u;     // rank in the cluster = value / score half
-    const int b = d.layer_sel >= 0 ? uc : uc / d.L;
-    const int l = d.layer_sel >= 0 ? d.layer_sel : uc % d.L;
-    const int32_t r = req_ids[b];
     const int k = d.k, S = d.S;
-    if (r < 0 || r >= d.R) {  // not a request: zero output (assemble would have rejected it); both CTAs leave
-        if (tid < kHeads) {
-            uint16_t* o = out + ((size_t)uc * kHeads + tid) * 512 + h * kVHalf;
-            for (int cc = 0; cc < kVHalf; cc += 8) *reinterpret_cast<uint4*>(o + cc) = make_uint4(0, 0, 0, 0);
-            if (h == 0 && lse) lse[(size_t)uc * kHeads + tid] = -INFINITY;
-        }
-        return;
-    }
+    const int nblk = (k + kBlk - 1) / kBlk;
+    // The cluster serves units cl, cl + ncl, ... in order; blocks are numbered across them (g), so the
+    // key pipeline, the exchanges and all phase arithmetic run on without a break between units.
+    auto req_of = [&](int u, int& b, int& l) -> int32_t {
+        b = d.layer_sel >= 0 ? u : u / d.L;
+        l = d.layer_sel >= 0 ? d.layer_sel : u % d.L;
+        const int32_t r = req_ids[b];
+        return r >= 0 && r < d.R ? r : -1;  // not a request: zero output (assemble would have rejected it)
+    };
     if (tc::smem_u32(smem) & 1023u) {  // the swizzled key stages need 1024-byte-aligned rows of atoms
         if (tid == 0) atomicOr(&d.ctl[CTL_ERR], DEVERR_TIMEOUT);
         return;  // both CTAs of the cluster see the same layout and leave together
     }
-    const int32_t* sl = slots + (size_t)uc * k;
-    const int nblk = (k + kBlk - 1) / kBlk;
+    int gtot = 0;  // blocks of this cluster's real units
+    for (int u = cl; u < units; u += ncl) {
+        int b, l;
+        if (req_of(u, b, l) >= 0) gtot += nblk;
+    }
     uint8_t* sK = smem;  // key stages
     uint8_t* sX = smem + lay.off_x;
     uint8_t* sP = smem + lay.off_p;
-    uint32_t* sMask = reinterpret_cast<uint32_t*>(smem + lay.off_mask);  // bit j of word 2i + g: key 64i + 32g + j is real
     volatile uint32_t* abort = &c.abort;
 
-    for (int g = warp; g < 2 * nblk; g += kAttnThreads / 32) {
-        const int key = 32 * g + lane;
-        const int32_t slot = key < k ? sl[key] : -1;
-        const uint32_t m = __ballot_sync(0xFFFFFFFFu, slot >= 0 && slot < S);
-        if (lane == 0) sMask[g] = m;
-    }
     if (tid == 0) {
         for (int s = 0; s < kMaxStages; ++s) {
             tc::mbar_init(&c.full[s], kLoadWarps);
@@ -310,13 +306,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
             tc::mbar_init(&c.pv_done[i], 1);
         }
         tc::mbar_init(&c.l_full, 1);
-        tc::mbar_init(&c.q_ready, kSoftmaxThreads);
+        tc::mbar_init(&c.q_ready, kSoftmaxThreads);  // the exchange warpgroup writes Q
+        tc::mbar_init(&c.o_free, kSoftmaxThreads);
         tc::mbar_init(&c.fin, 1);
         c.abort = 0u;
     }
     if (warp == kMmaWarp) tc::tmem_alloc(&c.tmem_base, kTmemCols);
     tc::fence_before_sync();
-    tc::cluster_sync();  // barriers of both CTAs exist before either sends to the other; masks staged
+    tc::cluster_sync();  // barriers of both CTAs exist before either sends to the other
     tc::fence_after_sync();
     const uint32_t tbase = c.tmem_base;
     // Register split (warpgroup-wide): softmax 192 a thread, exchange 72, MMA and loaders 88; the
@@ -329,58 +326,64 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
             // this CTA's 320-dim window; a masked slot is row -1, which reads zeros), lane j of warp w
             // issuing copy w + 7j -- TMA issue is paced per issuing thread, so the copies are spread over
             // as many lanes and warps as possible.  The warp fetches a block's 64 slots one block ahead
-            // (two a lane) and passes each lane its four rows by shuffle. ----
+            // (two a lane) and passes each lane its four rows by shuffle; loader 0 also warms L2 with the
+            // rows of the block nst ahead, whose stage frees up last. ----
             const int lw = warp - kLoadWarp0;
             const uint32_t mine = (uint32_t)((kGathers - lw + kLoadWarps - 1) / kLoadWarps);  // copies this loader issues
-            const int64_t row0 = ((int64_t)r * d.L + l) * S;                                 // first hot row of this unit
-            auto fetch = [&](int i, int half) -> int32_t {
-                const int key = i * kBlk + 32 * half + lane;
-                const int32_t slot = key < k ? sl[key] : -1;
-                return slot >= 0 && slot < S ? slot : -1;
-            };
-            int32_t v0 = fetch(0, 0), v1 = fetch(0, 1);
-            // loader 0 also warms L2 with the rows of block i + nst while block i is issued: when that
-            // block's stage frees up, its copies then come from L2 (the stage's life is the pipeline's
-            // limit); the slots of the block to warm are fetched one block ahead
-            const uint8_t* win = d.hot + (size_t)row0 * kRowBytes + 512u * h;  // this CTA's window of row 0
-            int32_t w0 = lw == 0 && nst < nblk ? fetch(nst, 0) : -1, w1 = lw == 0 && nst < nblk ? fetch(nst, 1) : -1;
             int last[kMaxStages] = {-1, -1, -1, -1};  // last block issued into each stage
             bool ok = true;
-            for (int i = 0; i < nblk; ++i) {
-                const int s = i % nst;
-                if (i >= nst && !(ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.empty[s], ((i / nst) - 1) & 1, abort))))
-                    break;
-                const int32_t n0 = i + 1 < nblk ? fetch(i + 1, 0) : -1, n1 = i + 1 < nblk ? fetch(i + 1, 1) : -1;
-                if (lane == 0) tc::mbar_arrive_expect_tx(&c.full[s], mine * 512u);
-                __syncwarp();
-                {   // lane j issues copy lw + 7j: one warp instruction for all of this warp's copies
-                    const int it = lw + kLoadWarps * lane;
-                    const int g = it / kWinBoxes, cb = it - g * kWinBoxes;
-                    int rr[4];
+            int g0 = 0;  // first block of the unit
+            for (int u = cl; ok && u < units; u += ncl) {
+                int b, l;
+                const int32_t r = req_of(u, b, l);
+                if (r < 0) continue;
+                const int64_t row0 = ((int64_t)r * d.L + l) * S;  // first hot row of this unit
+                const int32_t* sl = slots + (size_t)u * k;
+                auto fetch = [&](int i, int half) -> int32_t {
+                    const int key = i * kBlk + 32 * half + lane;
+                    const int32_t slot = key < k ? sl[key] : -1;
+                    return slot >= 0 && slot < S ? slot : -1;
+                };
+                const uint8_t* win = d.hot + (size_t)row0 * kRowBytes + 512u * h;  // this CTA's window of row 0
+                int32_t v0 = fetch(0, 0), v1 = fetch(0, 1);
+                int32_t w0 = lw == 0 && nst < nblk ? fetch(nst, 0) : -1, w1 = lw == 0 && nst < nblk ? fetch(nst, 1) : -1;
+                for (int i = 0; i < nblk; ++i) {
+                    const int g = g0 + i, s = g % nst;
+                    if (g >= nst && !(ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.empty[s], ((g / nst) - 1) & 1, abort))))
+                        break;
+                    const int32_t n0 = i + 1 < nblk ? fetch(i + 1, 0) : -1, n1 = i + 1 < nblk ? fetch(i + 1, 1) : -1;
+                    if (lane == 0) tc::mbar_arrive_expect_tx(&c.full[s], mine * 512u);
+                    __syncwarp();
+                    {   // lane j issues copy lw + 7j: one warp instruction for all of this warp's copies
+                        const int it = lw + kLoadWarps * lane;
+                        const int gr = it / kWinBoxes, cb = it - gr * kWinBoxes;
+                        int rr[4];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int j = (4 * g + u) & (kBlk - 1);  // key of the block
-                        const int32_t a = __shfl_sync(0xFFFFFFFFu, v0, j & 31), b2 = __shfl_sync(0xFFFFFFFFu, v1, j & 31);
-                        const int32_t slot = j < 32 ? a : b2;
-                        rr[u] = slot >= 0 ? (int)(row0 + slot) : -1;
+                        for (int x = 0; x < 4; ++x) {
+                            const int j = (4 * gr + x) & (kBlk - 1);  // key of the block
+                            const int32_t a = __shfl_sync(0xFFFFFFFFu, v0, j & 31), b2 = __shfl_sync(0xFFFFFFFFu, v1, j & 31);
+                            const int32_t slot = j < 32 ? a : b2;
+                            rr[x] = slot >= 0 ? (int)(row0 + slot) : -1;
+                        }
+                        if ((uint32_t)lane < mine)
+                            tc::tma_gather4(tc::smem_u32(sK + s * kStageBytes) + cb * kBoxBytes + gr * 512u, &hot_map,
+                                            256 * (int)h + 64 * cb, rr[0], rr[1], rr[2], rr[3], &c.full[s]);
                     }
-                    if ((uint32_t)lane < mine)
-                        tc::tma_gather4(tc::smem_u32(sK + s * kStageBytes) + cb * kBoxBytes + g * 512u, &hot_map,
-                                        256 * (int)h + 64 * cb, rr[0], rr[1], rr[2], rr[3], &c.full[s]);
-                }
-                if (lw == 0 && i + nst < nblk) {
+                    if (lw == 0 && i + nst < nblk) {
 #pragma unroll
-                    for (int cb = 0; cb < kWinBoxes; ++cb) {
-                        if (w0 >= 0) tc::prefetch_l2(win + (size_t)w0 * kRowBytes + 128 * cb);
-                        if (w1 >= 0) tc::prefetch_l2(win + (size_t)w1 * kRowBytes + 128 * cb);
+                        for (int cb = 0; cb < kWinBoxes; ++cb) {
+                            if (w0 >= 0) tc::prefetch_l2(win + (size_t)w0 * kRowBytes + 128 * cb);
+                            if (w1 >= 0) tc::prefetch_l2(win + (size_t)w1 * kRowBytes + 128 * cb);
+                        }
+                        const bool more = i + nst + 1 < nblk;
+                        w0 = more ? fetch(i + nst + 1, 0) : -1;
+                        w1 = more ? fetch(i + nst + 1, 1) : -1;
                     }
-                    const bool more = i + nst + 1 < nblk;
-                    w0 = more ? fetch(i + nst + 1, 0) : -1;
-                    w1 = more ? fetch(i + nst + 1, 1) : -1;
+                    last[s] = g;
+                    v0 = n0;
+                    v1 = n1;
                 }
-                last[s] = i;
-                v0 = n0;
-                v1 = n1;
+                g0 += nblk;
             }
             if (lane == 0) {
                 if (!ok) give_up(c, &d.ctl[CTL_ERR]);
@@ -390,20 +393,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
             }
             __syncwarp();
         } else {
-            // ---- MMA issuer: whichever product is ready first.  O += P(i) V(i) as soon as P(i) is
-            // complete (it frees the key stage for the loaders); S(j) as soon as its keys have landed
-            // and S(j-1) has been read out of tensor memory.  Both streams are issued in order. ----
+            // ---- MMA issuer: whichever product is ready first.  O += P(g) V(g) as soon as P(g) is
+            // complete (it frees the key stage for the loaders) and, for a unit's first block, once the
+            // softmax has read the previous unit's accumulator; S(g) as soon as its keys have landed,
+            // S(g-1) has been read out of tensor memory and its unit's Q is in place.  Both streams are
+            // issued in order. ----
             if (lane == 0) {
                 const uint32_t idesc_s = tc::idesc_bf16_f32(kHeads, kBlk, 0);
                 const uint32_t idesc_o = tc::idesc_bf16_f32(kHeads, kVHalf, 1);
                 const uint32_t aK = tc::smem_u32(sK), aP = tc::smem_u32(sP);
-                bool ok = wait_phase(&c.q_ready, 0, abort);
-                tc::fence_after_sync();
-                int js = 0, ipv = 0;  // next S block, next P V block
+                bool ok = true;
+                int js = 0, ipv = 0, qn = 0;  // next S block, next P V block, units whose Q is in place
                 uint32_t idle = 0;
-                while (ok && ipv < nblk) {
+                while (ok && ipv < gtot) {
                     bool progressed = false;
-                    if (ipv < js && tc::mbar_ready(tc::smem_u32(&c.p_full[ipv & 1]), (uint32_t)(ipv >> 1) & 1u)) {
+                    const int pu = ipv / nblk, pi = ipv - pu * nblk;  // unit and block of the next P V
+                    if (ipv < js && tc::mbar_ready(tc::smem_u32(&c.p_full[ipv & 1]), (uint32_t)(ipv >> 1) & 1u) &&
+                        (pi > 0 || pu == 0 || tc::mbar_ready(tc::smem_u32(&c.o_free), (uint32_t)(pu - 1) & 1u))) {
                         const int bb = ipv & 1, s = ipv % nst;
                         tc::fence_smem_async();  // the peer's half arrived through the generic proxy
                         tc::fence_after_sync();
@@ -412,13 +418,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
                         for (int st = 0; st < kBlk / 16; ++st)
                             tc::mma_bf16(tbase + kColO, tc::kmajor_desc(aP + bb * kPBytes + 256u * st, kBlk),
                                          tc::sw128_mnmajor_desc(vst + 2048u * st, kBoxBytes), idesc_o,
-                                         (ipv > 0 || st > 0) ? 1u : 0u);
+                                         (pi > 0 || st > 0) ? 1u : 0u);
                         tc::mma_commit(&c.pv_done[bb]);
                         tc::mma_commit(&c.empty[s]);
                         ++ipv;
                         progressed = true;
                     }
-                    if (js < nblk && tc::mbar_ready(tc::smem_u32(&c.full[js % nst]), (uint32_t)(js / nst) & 1u) &&
+                    if (js < gtot && js / nblk == qn && tc::mbar_ready(tc::smem_u32(&c.q_ready), (uint32_t)qn & 1u))
+                        ++qn;
+                    if (js < gtot && js / nblk < qn &&
+                        tc::mbar_ready(tc::smem_u32(&c.full[js % nst]), (uint32_t)(js / nst) & 1u) &&
                         (js == 0 || tc::mbar_ready(tc::smem_u32(&c.s_empty), (uint32_t)(js - 1) & 1u))) {
                         const int s = js % nst;
                         tc::fence_after_sync();
@@ -449,11 +458,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
             __syncwarp();
         }
     } else if (warp >= kXchgWarp0) {
-        // ---- exchange warpgroup: thread t <-> head t.  For every block, the peer's 32 keys of my
-        // partial S go straight from tensor memory into the peer's exchange tile (st.async; the bytes
-        // complete on the peer's x_full).  Block j is sent only once my softmax has taken block
-        // j - 2's maxima -- which it cannot do before the peer has read block j - 2's tile, the
-        // previous user of the buffer. ----
+        // ---- exchange warpgroup: thread t <-> head t.  Per unit it first writes the unit's Q into
+        // tensor memory (every score product of the previous unit has completed: this warpgroup
+        // waited for the last one).  For every block, the peer's 32 keys of my partial S go straight
+        // from tensor memory into the peer's exchange tile (st.async; the bytes complete on the
+        // peer's x_full).  Block g is sent only once my softmax has taken block g - 2's maxima -- which
+        // it cannot do before the peer has read block g - 2's tile, the previous user of the buffer. ----
         tc::regs_shrink<kXchgRegs>();
         const int hd = tid - kSoftmaxThreads;
         const uint32_t tl = tbase + ((uint32_t)((warp & 3) * 32) << 16);
@@ -461,19 +471,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
         const uint32_t xf0 = tc::map_to_rank(tc::smem_u32(&c.x_full[0]), peer);
         const uint32_t xf1 = tc::map_to_rank(tc::smem_u32(&c.x_full[1]), peer);
         bool ok = true;
-        for (int j = 0; ok && j < nblk; ++j) {
-            if (j >= 2 && !(ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.adv, (uint32_t)(j - 2) & 1u, abort)))) break;
-            if (!(ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.s_full, (uint32_t)j & 1u, abort)))) break;
-            tc::fence_after_sync();
-            float v[kHalfBlk];
-            tc::tmem_ld32(tl + kColS + (uint32_t)(kHalfBlk * peer), v);
-            tc::fence_before_sync();
-            tc::mbar_arrive(&c.s_empty);
-            const uint32_t xb = x_peer + (uint32_t)(j & 1) * kXBytes;
-            const uint32_t rb = (j & 1) ? xf1 : xf0;
+        int g0 = 0;
+        for (int u = cl; ok && u < units; u += ncl) {
+            int b, l;
+            if (req_of(u, b, l) < 0) continue;
+            {   // Q of the unit: this head's 288 score dims into columns [kColQ, kColQ + 144)
+                const uint4* qr = reinterpret_cast<const uint4*>(q + ((size_t)u * kHeads + hd) * kDim + h * kQKHalf);
+#pragma unroll 3
+                for (int gq = 0; gq < kQKHalf / 32; ++gq) {  // 9 groups of 16 columns
+                    uint4 a = qr[4 * gq], bq = qr[4 * gq + 1], cq4 = qr[4 * gq + 2], dq = qr[4 * gq + 3];
+                    const uint32_t w0[8] = {a.x, a.y, a.z, a.w, bq.x, bq.y, bq.z, bq.w};
+                    const uint32_t w1[8] = {cq4.x, cq4.y, cq4.z, cq4.w, dq.x, dq.y, dq.z, dq.w};
+                    tc::tmem_st8_async(tl + kColQ + 16u * gq, w0);
+                    tc::tmem_st8_async(tl + kColQ + 16u * gq + 8u, w1);
+                }
+                tc::tmem_wait_st();
+                tc::fence_before_sync();
+                tc::mbar_arrive(&c.q_ready);
+                if (u + ncl < units) {  // warm L2 with the next unit's Q row
+                    const uint8_t* nq = reinterpret_cast<const uint8_t*>(q + ((size_t)(u + ncl) * kHeads + hd) * kDim + h * kQKHalf);
 #pragma unroll
-            for (int m = 0; m < kHalfBlk / 4; ++m)
-                tc::st_async16(xb + 2048u * m, v[4 * m], v[4 * m + 1], v[4 * m + 2], v[4 * m + 3], rb);
+                    for (int x = 0; x < 5; ++x) tc::prefetch_l2(nq + 128 * x);
+                }
+            }
+            for (int i = 0; ok && i < nblk; ++i) {
+                const int g = g0 + i;
+                if (g >= 2 && !(ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.adv, (uint32_t)(g - 2) & 1u, abort)))) break;
+                if (!(ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.s_full, (uint32_t)g & 1u, abort)))) break;
+                tc::fence_after_sync();
+                float v[kHalfBlk];
+                tc::tmem_ld32(tl + kColS + (uint32_t)(kHalfBlk * peer), v);
+                tc::fence_before_sync();
+                tc::mbar_arrive(&c.s_empty);
+                const uint32_t xb = x_peer + (uint32_t)(g & 1) * kXBytes;
+                const uint32_t rb = (g & 1) ? xf1 : xf0;
+#pragma unroll
+                for (int m = 0; m < kHalfBlk / 4; ++m)
+                    tc::st_async16(xb + 2048u * m, v[4 * m], v[4 * m + 1], v[4 * m + 2], v[4 * m + 3], rb);
+            }
+            g0 += nblk;
         }
         if (!ok) give_up(c, &d.ctl[CTL_ERR]);
     } else {
@@ -483,26 +519,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
         tc::regs_grow<kSoftmaxRegs>();
         const int hd = tid;
         const uint32_t tl = tbase + ((uint32_t)(warp * 32) << 16);
-        {   // Q: this head's 288 score dims into columns [kColQ, kColQ + 144)
-            const uint4* qr = reinterpret_cast<const uint4*>(q + ((size_t)uc * kHeads + hd) * kDim + h * kQKHalf);
-#pragma unroll 3
-            for (int g = 0; g < kQKHalf / 32; ++g) {  // 9 groups of 16 columns
-                uint4 a = qr[4 * g], bq = qr[4 * g + 1], cq4 = qr[4 * g + 2], dq = qr[4 * g + 3];
-                const uint32_t w0[8] = {a.x, a.y, a.z, a.w, bq.x, bq.y, bq.z, bq.w};
-                const uint32_t w1[8] = {cq4.x, cq4.y, cq4.z, cq4.w, dq.x, dq.y, dq.z, dq.w};
-                tc::tmem_st8_async(tl + kColQ + 16u * g, w0);
-                tc::tmem_st8_async(tl + kColQ + 16u * g + 8u, w1);
-            }
-            tc::tmem_wait_st();
-            tc::fence_before_sync();
-            tc::mbar_arrive(&c.q_ready);
-        }
         const uint32_t mx_peer = tc::map_to_rank(tc::smem_u32(&c.mx[0][0]), peer) + (uint32_t)hd * 4u;
         const uint32_t mf0 = tc::map_to_rank(tc::smem_u32(&c.m_full[0]), peer);
         const uint32_t mf1 = tc::map_to_rank(tc::smem_u32(&c.m_full[1]), peer);
         const uint32_t p_peer = tc::map_to_rank(tc::smem_u32(sP), peer);
         const uint32_t pf0 = tc::map_to_rank(tc::smem_u32(&c.p_full[0]), peer);
         const uint32_t pf1 = tc::map_to_rank(tc::smem_u32(&c.p_full[1]), peer);
+        const uint32_t lx_peer = tc::map_to_rank(tc::smem_u32(&c.lx[0]), peer) + (uint32_t)hd * 4u;
+        const uint32_t lf_peer = tc::map_to_rank(tc::smem_u32(&c.l_full), peer);
         auto own = [&](int j, float (&dst)[kHalfBlk]) -> bool {  // my keys of my partial S(j)
             if (!__all_sync(0xFFFFFFFFu, wait_phase(&c.s_full, (uint32_t)j & 1u, abort))) return false;
             tc::fence_after_sync();
@@ -511,126 +535,151 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
             tc::mbar_arrive(&c.s_empty);
             return true;
         };
-        float m_ref = -INFINITY;  // reference maximum (log2 domain) the exponentials use; equal in both CTAs
-        float l_run = 0.0f;       // this CTA's share of the softmax denominator
-        float cur[kHalfBlk];      // my partial S of the block being processed, my keys
-        if (tid == 0) tc::mbar_arrive_expect_tx(&c.x_full[0], kXBytes);
-        bool ok = own(0, cur);
-        for (int i = 0; ok && i < nblk; ++i) {
-            const int bb = i & 1;
-            const uint32_t ph = (uint32_t)(i >> 1) & 1u;
-            if (!(ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.x_full[bb], ph, abort)))) break;
-            float sv[kHalfBlk];  // mine + the peer's partial: the full scores of my keys
-            const uint8_t* xrow = sX + bb * kXBytes + hd * 16;
+        float cur[kHalfBlk];  // my partial S of the block being processed, my keys
+        bool ok = true;
+        if (gtot > 0) {
+            if (tid == 0) tc::mbar_arrive_expect_tx(&c.x_full[0], kXBytes);
+            ok = own(0, cur);
+        }
+        int g0 = 0, n = 0;  // first block of the unit; units done
+        for (int u = cl; u < units; u += ncl) {
+            int b, l;
+            if (req_of(u, b, l) < 0) {  // not a request: zeros and lse = -inf, nothing else takes part
+                uint16_t* o = out + ((size_t)u * kHeads + hd) * 512 + h * kVHalf;
+                for (int cc = 0; cc < kVHalf; cc += 8) *reinterpret_cast<uint4*>(o + cc) = make_uint4(0, 0, 0, 0);
+                if (h == 0 && lse) lse[(size_t)u * kHeads + hd] = -INFINITY;
+                continue;
+            }
+            if (!ok) continue;
+            const int32_t* sl = slots + (size_t)u * k;
+            auto slot_of = [&](int i) -> int32_t {  // the slot of my key `lane` of block i
+                const int key = i * kBlk + kHalfBlk * (int)h + lane;
+                return key < k ? sl[key] : -1;
+            };
+            float m_ref = -INFINITY;  // reference maximum (log2 domain) the exponentials use; equal in both CTAs
+            float l_run = 0.0f;       // this CTA's share of the softmax denominator
+            int32_t sp = slot_of(0);
+            for (int i = 0; ok && i < nblk; ++i) {
+                const int g = g0 + i, bb = g & 1;
+                const uint32_t ph = (uint32_t)(g >> 1) & 1u;
+                if (!(ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.x_full[bb], ph, abort)))) break;
+                float sv[kHalfBlk];  // mine + the peer's partial: the full scores of my keys
+                const uint8_t* xrow = sX + bb * kXBytes + hd * 16;
 #pragma unroll
-            for (int m = 0; m < kHalfBlk / 4; ++m) {
-                const float4 pr = *reinterpret_cast<const float4*>(xrow + 2048 * m);
-                sv[4 * m] = cur[4 * m] + pr.x;
-                sv[4 * m + 1] = cur[4 * m + 1] + pr.y;
-                sv[4 * m + 2] = cur[4 * m + 2] + pr.z;
-                sv[4 * m + 3] = cur[4 * m + 3] + pr.w;
-            }
-            if (i + 1 < nblk) {
-                if (tid == 0) tc::mbar_arrive_expect_tx(&c.x_full[bb ^ 1], kXBytes);
-                if (!(ok = own(i + 1, cur))) break;
-            }
-            const uint32_t vm = sMask[2 * i + h];
-            if (vm != 0xFFFFFFFFu) {
+                for (int m = 0; m < kHalfBlk / 4; ++m) {
+                    const float4 pr = *reinterpret_cast<const float4*>(xrow + 2048 * m);
+                    sv[4 * m] = cur[4 * m] + pr.x;
+                    sv[4 * m + 1] = cur[4 * m + 1] + pr.y;
+                    sv[4 * m + 2] = cur[4 * m + 2] + pr.z;
+                    sv[4 * m + 3] = cur[4 * m + 3] + pr.w;
+                }
+                const int32_t sp_next = i + 1 < nblk ? slot_of(i + 1) : -1;  // in flight while this block runs
+                if (g + 1 < gtot) {  // S of the next block, possibly of the next unit
+                    if (tid == 0) tc::mbar_arrive_expect_tx(&c.x_full[bb ^ 1], kXBytes);
+                    if (!(ok = own(g + 1, cur))) break;
+                }
+                const uint32_t vm = __ballot_sync(0xFFFFFFFFu, sp >= 0 && sp < S);
+                if (vm != 0xFFFFFFFFu) {
 #pragma unroll
-                for (int j = 0; j < kHalfBlk; ++j) sv[j] = (vm >> j) & 1u ? sv[j] : -INFINITY;
-            }
-            float mx[4];
+                    for (int j = 0; j < kHalfBlk; ++j) sv[j] = (vm >> j) & 1u ? sv[j] : -INFINITY;
+                }
+                float mx[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                mx[j] = fmaxf(fmaxf(fmaxf(sv[j], sv[j + 4]), fmaxf(sv[j + 8], sv[j + 12])),
-                              fmaxf(fmaxf(sv[j + 16], sv[j + 20]), fmaxf(sv[j + 24], sv[j + 28])));
-            const float mloc = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-            // P tile bb (mine and, once I send my maxima, the peer's half) is free once O += P(i-2) V(i-2)
-            // has completed; the peer sends its P(i) only after my maxima of block i
-            if (i >= 2 && !(ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.pv_done[bb], ((i - 2) >> 1) & 1, abort))))
-                break;
-            if (tid == 0) tc::mbar_arrive_expect_tx(&c.m_full[bb], kHeads * 4u);
-            tc::st_async4(mx_peer + (uint32_t)bb * kHeads * 4u, mloc, bb ? mf1 : mf0);
-            if (!(ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.m_full[bb], ph, abort)))) break;
-            const float mb = fmaxf(mloc, c.mx[bb][hd]) * scale_log2;  // the same in both CTAs
-            tc::mbar_arrive(&c.adv);  // the exchange warpgroup may now send block i + 2
-            float factor = 1.0f;
-            if (mb > m_ref + kRescaleLog2) {
-                factor = m_ref == -INFINITY ? 0.0f : ex2(m_ref - mb);
-                m_ref = mb;
-                l_run *= factor;
-            }
-            if (i > 0 && __any_sync(0xFFFFFFFFu, factor != 1.0f)) {  // rescale this warp's rows of O
-                if (!(ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, abort))))
+                for (int j = 0; j < 4; ++j)
+                    mx[j] = fmaxf(fmaxf(fmaxf(sv[j], sv[j + 4]), fmaxf(sv[j + 8], sv[j + 12])),
+                                  fmaxf(fmaxf(sv[j + 16], sv[j + 20]), fmaxf(sv[j + 24], sv[j + 28])));
+                const float mloc = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+                // P tile bb (mine and, once I send my maxima, the peer's half) is free once O += P(g-2)
+                // V(g-2) has completed; the peer sends its P(g) only after my maxima of block g
+                if (g >= 2 && !(ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.pv_done[bb], ((g - 2) >> 1) & 1, abort))))
                     break;
+                if (tid == 0) tc::mbar_arrive_expect_tx(&c.m_full[bb], kHeads * 4u);
+                tc::st_async4(mx_peer + (uint32_t)bb * kHeads * 4u, mloc, bb ? mf1 : mf0);
+                if (!(ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.m_full[bb], ph, abort)))) break;
+                const float mb = fmaxf(mloc, c.mx[bb][hd]) * scale_log2;  // the same in both CTAs
+                tc::mbar_arrive(&c.adv);  // the exchange warpgroup may now send block g + 2
+                float factor = 1.0f;
+                if (mb > m_ref + kRescaleLog2) {
+                    factor = m_ref == -INFINITY ? 0.0f : ex2(m_ref - mb);
+                    m_ref = mb;
+                    l_run *= factor;
+                }
+                if (i > 0 && __any_sync(0xFFFFFFFFu, factor != 1.0f)) {  // rescale this warp's rows of O
+                    if (!(ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, abort))))
+                        break;
+                    tc::fence_after_sync();
+                    for (int c0 = 0; c0 < kVHalf; c0 += 32) {
+                        float ov[32];
+                        tc::tmem_ld32(tl + kColO + c0, ov);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) ov[j] *= factor;
+                        tc::tmem_st32(tl + kColO + c0, ov);
+                    }
+                    tc::fence_before_sync();
+                }
+                // p = 2^(s * scale - m_ref); masked keys give 2^-inf = 0.  While no
+                // real key has been seen (m_ref = -inf for every head) all p are 0.
+                uint32_t pk[kHalfBlk / 2];
+                float ps[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                if (m_ref != -INFINITY) {
+                    const float neg_m = -m_ref;
+#pragma unroll
+                    for (int j = 0; j < kHalfBlk; j += 2) {
+                        const float p0 = ex2(fmaf(sv[j], scale_log2, neg_m));
+                        const float p1 = ex2(fmaf(sv[j + 1], scale_log2, neg_m));
+                        ps[(j >> 1) & 3] += p0 + p1;
+                        pk[j / 2] = bf2(p0, p1);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < kHalfBlk / 2; ++j) pk[j] = 0u;
+                }
+                l_run += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+                // my half of P(g): into my tile and into the peer's, at the same place (keys [32h, 32h + 32))
+                const uint32_t pb = (uint32_t)bb * kPBytes;
+#pragma unroll
+                for (int cc = 0; cc < kHalfBlk / 8; ++cc) {
+                    const uint32_t off = pb + tc::kmajor_chunk_offset(hd, 4 * h + cc, kBlk);
+                    const uint4 w4 = make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+                    *reinterpret_cast<uint4*>(sP + off) = w4;
+                    tc::st_async16u(p_peer + off, w4, bb ? pf1 : pf0);
+                }
+                tc::fence_smem_async();
+                if (tid == 0)
+                    tc::mbar_arrive_expect_tx(&c.p_full[bb], kPBytes / 2);  // my arrival + the peer's half
+                else
+                    tc::mbar_arrive(&c.p_full[bb]);
+                sp = sp_next;
+            }
+            const int gl = g0 + nblk - 1;  // the unit's last block
+            if (ok) ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.pv_done[gl & 1], ((gl >> 1) & 1), abort));
+            // the denominator: CTA 0's share + CTA 1's share, in that order on both CTAs
+            if (tid == 0) tc::mbar_arrive_expect_tx(&c.l_full, kHeads * 4u);
+            tc::st_async4(lx_peer, l_run, lf_peer);
+            if (ok) ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.l_full, (uint32_t)n & 1u, abort));
+            if (ok) {
+                const float l_all = h == 0 ? l_run + c.lx[hd] : c.lx[hd] + l_run;
                 tc::fence_after_sync();
+                uint16_t* o = out + ((size_t)u * kHeads + hd) * 512 + h * kVHalf;
+                const float inv = l_all > 0.0f ? 1.0f / l_all : 0.0f;
                 for (int c0 = 0; c0 < kVHalf; c0 += 32) {
                     float ov[32];
                     tc::tmem_ld32(tl + kColO + c0, ov);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) ov[j] *= factor;
-                    tc::tmem_st32(tl + kColO + c0, ov);
+                    for (int cc = 0; cc < 4; ++cc)
+                        *reinterpret_cast<uint4*>(o + c0 + 8 * cc) =
+                            make_uint4(bf2(ov[8 * cc] * inv, ov[8 * cc + 1] * inv), bf2(ov[8 * cc + 2] * inv, ov[8 * cc + 3] * inv),
+                                       bf2(ov[8 * cc + 4] * inv, ov[8 * cc + 5] * inv), bf2(ov[8 * cc + 6] * inv, ov[8 * cc + 7] * inv));
                 }
+                if (h == 0 && lse)
+                    lse[(size_t)u * kHeads + hd] = l_all > 0.0f ? (m_ref + log2f(l_all)) * 0.69314718055994531f : -INFINITY;
                 tc::fence_before_sync();
+                tc::mbar_arrive(&c.o_free);  // the next unit's first O += P V may overwrite the accumulator
             }
-            // p = 2^(s * scale - m_ref); masked keys give 2^-inf = 0.  While no
-            // real key has been seen (m_ref = -inf for every head) all p are 0.
-            uint32_t pk[kHalfBlk / 2];
-            float ps[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            if (m_ref != -INFINITY) {
-                const float neg_m = -m_ref;
-#pragma unroll
-                for (int j = 0; j < kHalfBlk; j += 2) {
-                    const float p0 = ex2(fmaf(sv[j], scale_log2, neg_m));
-                    const float p1 = ex2(fmaf(sv[j + 1], scale_log2, neg_m));
-                    ps[(j >> 1) & 3] += p0 + p1;
-                    pk[j / 2] = bf2(p0, p1);
-                }
-            } else {
-#pragma unroll
-                for (int j = 0; j < kHalfBlk / 2; ++j) pk[j] = 0u;
-            }
-            l_run += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-            // my half of P(i): into my tile and into the peer's, at the same place (keys [32h, 32h + 32))
-            const uint32_t pb = (uint32_t)bb * kPBytes;
-#pragma unroll
-            for (int cc = 0; cc < kHalfBlk / 8; ++cc) {
-                const uint32_t off = pb + tc::kmajor_chunk_offset(hd, 4 * h + cc, kBlk);
-                const uint4 w4 = make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-                *reinterpret_cast<uint4*>(sP + off) = w4;
-                tc::st_async16u(p_peer + off, w4, bb ? pf1 : pf0);
-            }
-            tc::fence_smem_async();
-            if (tid == 0)
-                tc::mbar_arrive_expect_tx(&c.p_full[bb], kPBytes / 2);  // my arrival + the peer's half
-            else
-                tc::mbar_arrive(&c.p_full[bb]);
+            g0 += nblk;
+            ++n;
         }
-        if (ok && nblk > 0) ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.pv_done[(nblk - 1) & 1], ((nblk - 1) >> 1) & 1, abort));
-        // the denominator: CTA 0's share + CTA 1's share, in that order on both CTAs
-        if (tid == 0) tc::mbar_arrive_expect_tx(&c.l_full, kHeads * 4u);
-        tc::st_async4(tc::map_to_rank(tc::smem_u32(&c.lx[0]), peer) + (uint32_t)hd * 4u, l_run,
-                      tc::map_to_rank(tc::smem_u32(&c.l_full), peer));
-        if (ok) ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.l_full, 0u, abort));
-        if (ok) {
-            const float l_all = h == 0 ? l_run + c.lx[hd] : c.lx[hd] + l_run;
-            tc::fence_after_sync();
-            uint16_t* o = out + ((size_t)uc * kHeads + hd) * 512 + h * kVHalf;
-            const float inv = l_all > 0.0f ? 1.0f / l_all : 0.0f;
-            for (int c0 = 0; c0 < kVHalf; c0 += 32) {
-                float ov[32];
-                tc::tmem_ld32(tl + kColO + c0, ov);
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc)
-                    *reinterpret_cast<uint4*>(o + c0 + 8 * cc) =
-                        make_uint4(bf2(ov[8 * cc] * inv, ov[8 * cc + 1] * inv), bf2(ov[8 * cc + 2] * inv, ov[8 * cc + 3] * inv),
-                                   bf2(ov[8 * cc + 4] * inv, ov[8 * cc + 5] * inv), bf2(ov[8 * cc + 6] * inv, ov[8 * cc + 7] * inv));
-            }
-            if (h == 0 && lse)
-                lse[(size_t)uc * kHeads + hd] = l_all > 0.0f ? (m_ref + log2f(l_all)) * 0.69314718055994531f : -INFINITY;
-        } else {
-            give_up(c, &d.ctl[CTL_ERR]);
-        }
+        if (!ok) give_up(c, &d.ctl[CTL_ERR]);
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -643,7 +692,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
 
 }  // namespace
 
-size_t attend_smem_bytes(int k) { return attend_layout(k).bytes; }
+size_t attend_smem_bytes(int) { return attend_layout().bytes; }
 
 // The hot buffer as a 2-D tensor of R*L*S rows by 576 bf16 (row stride 1152
 // bytes) for TMA: box one row by 64 columns, 128-byte swizzle, out-of-range
@@ -681,11 +730,20 @@ cudaError_t launch_attend(const void* hot_map, const Dev& d, const int32_t* req_
     static const cudaError_t attr = cudaFuncSetAttribute(attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                          (int)kSmemLimit);
     if (attr != cudaSuccess) return attr;
-    const AttnLayout lay = attend_layout(d.k);
+    const AttnLayout lay = attend_layout();
     if (d.k > (int)kMaxTopk || lay.bytes > kSmemLimit) return cudaErrorInvalidValue;
-    attend_kernel<<<call_units(d, B) * 2, kAttnThreads, lay.bytes, st>>>(
+    static int sms = 0;  // a persistent grid: one cluster per two SMs (one CTA per SM), at most one per unit
+    if (sms == 0) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+    }
+    const int units = call_units(d, B);
+    const int clusters = std::max(1, std::min(units, sms / 2));
+    attend_kernel<<<clusters * 2, kAttnThreads, lay.bytes, st>>>(
         *static_cast<const CUtensorMap*>(hot_map), d, req_ids, static_cast<const uint16_t*>(q), slots,
-        static_cast<uint16_t*>(out), lse, sm_scale * 1.4426950408889634f, lay);
+        static_cast<uint16_t*>(out), lse, sm_scale * 1.4426950408889634f, lay, units);
     return cudaGetLastError();
 }
 
