@@ -52,6 +52,9 @@ def parse():
     ap.add_argument("--pipeline", action="store_true",
                     help="with --attend: layer by layer, attention of layer l on a second stream overlapping the "
                          "assembly of layer l+1")
+    ap.add_argument("--attend-sms", type=int, default=0,
+                    help="with --attend: SMs the attention kernel may occupy (0: all), leaving the rest to the "
+                         "assembly running beside it (--pipeline)")
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--cpu-sample-requests", type=int, default=32)
     ap.add_argument("--cpu-sample-steps", type=int, default=24)
@@ -335,6 +338,7 @@ def run_ours(args):
     if args.pipeline and not layered:
         raise SystemExit("--pipeline needs --layered")
     if attn_on:
+        ctx.set_attend_sms(args.attend_sms)
         # synthetic decode queries (128 heads x 576) per unit, fixed across steps
         units = [(b, l) for l in range(w.L) for b in range(w.B)] if layered else \
                 [(b, l) for b in range(w.B) for l in range(w.L)]
@@ -433,8 +437,9 @@ def run_ours(args):
     st1 = ctx.stats()
     M = st1["misses"] - st0["misses"]
     H = st1["hits"] - st0["hits"]
-    assert st1["calls"] - st0["calls"] == K * per_call
-    assert ctx.get_device_error() == 0
+    dev_err = ctx.get_device_error()
+    assert st1["calls"] - st0["calls"] == K * per_call and dev_err == 0, \
+        f"{st1['calls'] - st0['calls']} of {K * per_call} timed calls succeeded; device error bits {dev_err}"
     gather_s = sum(event_ms(ev_b[e], ev_a[e]) for e in range(W * per_call, n_dev * per_call)) / 1e3
     per_step_m = misses[W:].sum(dim=(1, 2)).cpu().numpy().astype(np.int64)
     per_step_h = hits[W:].sum(dim=(1, 2)).cpu().numpy().astype(np.int64)
@@ -515,7 +520,7 @@ def run_ours(args):
                        "hot_slots": w.S, "fresh": w.fresh, "row_bytes": rb, "row_dtype": "bf16",
                        "write_back_per_step": w.appends, "cuda_graph": use_graph,
                        "layered": layered, "turn_every": w.turn_every, "turn_tokens": w.turn_tokens,
-                       "attend": attn_on, "pipeline": bool(args.pipeline),
+                       "attend": attn_on, "pipeline": bool(args.pipeline), "attend_sms": args.attend_sms,
                        "l2": "inputs larger than L2: each step writes the missed rows (~0.6 GB) into a "
                              f"{w.hot_bytes() / 1e9:.2f} GB hot buffer and reads {w.B * w.L * w.max_context * 4 / 1e6:.0f} MB "
                              "of token->slot maps; no flush"},

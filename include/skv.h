@@ -308,6 +308,15 @@ SKV_API skv_status skv_get_stats(skv_ctx *ctx, uint64_t *calls, uint64_t *hits, 
  * SKV_ERR_INVALID_ARG.  The events belong to the caller. */
 SKV_API skv_status skv_set_gather_events(skv_ctx *ctx, skv_event_t before, skv_event_t after);
 
+/* Optional: the attention kernel of later skv_attend calls on this context
+ * occupies at most `sms` SMs (one CTA per SM, in clusters of two; rounded
+ * down to an even count, at least 2), leaving the others to work running at
+ * the same time on other streams -- e.g. the next layer's skv_assemble_layer,
+ * which is bound by the host link and needs few SMs to keep it busy.  0 (the
+ * default) uses every SM.  Negative: SKV_ERR_INVALID_ARG.  Results do not
+ * depend on it. */
+SKV_API skv_status skv_set_attend_sms(skv_ctx *ctx, int32_t sms);
+
 /* Diagnostic: one 128 x n x k bf16 matrix product on the tensor cores through
  * the same path the attention consumer uses (tcgen05 MMA into tensor memory,
  * read back by the issuing warpgroup):

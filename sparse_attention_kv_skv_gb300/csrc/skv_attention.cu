@@ -217,7 +217,9 @@ struct alignas(16) AttnCtl {
     uint64_t empty[kMaxStages];  // key stage consumed by its last product
     uint64_t s_full;             // partial S of the next block is in tensor memory
     uint64_t s_empty;            // the softmax and exchange warpgroups have read it
-    uint64_t adv;                // the softmax warpgroup has taken a block's row maxima (one phase a block)
+    uint64_t adv[2];             // the softmax warpgroup has taken block g's row maxima (adv[g % 2]: a phase
+                                 // every second block, so a waiter that falls behind by a block still sees
+                                 // its phase -- a parity wait tells only the current and the previous one)
     uint64_t x_full[2];          // the peer's partial scores of my keys of a block have arrived (16384 bytes)
     uint64_t m_full[2];          // the peer's row maxima of a block have arrived (512 bytes)
     uint64_t p_full[2];          // a P tile is complete: my half written, the peer's half arrived (8192 bytes)
@@ -298,8 +300,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
         }
         tc::mbar_init(&c.s_full, 1);
         tc::mbar_init(&c.s_empty, 2 * kSoftmaxThreads);  // the softmax and the exchange warpgroups
-        tc::mbar_init(&c.adv, kSoftmaxThreads);
         for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&c.adv[i], kSoftmaxThreads);
             tc::mbar_init(&c.x_full[i], 1);                // one expect_tx arrival + the peer's bytes
             tc::mbar_init(&c.m_full[i], 1);
             tc::mbar_init(&c.p_full[i], kSoftmaxThreads);  // my half (one of them with expect_tx) + the peer's bytes
@@ -496,7 +498,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
             }
             for (int i = 0; ok && i < nblk; ++i) {
                 const int g = g0 + i;
-                if (g >= 2 && !(ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.adv, (uint32_t)(g - 2) & 1u, abort)))) break;
+                if (g >= 2 && !(ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.adv[g & 1], (uint32_t)((g - 2) >> 1) & 1u, abort))))
+                    break;
                 if (!(ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.s_full, (uint32_t)g & 1u, abort)))) break;
                 tc::fence_after_sync();
                 float v[kHalfBlk];
@@ -597,7 +600,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
                 tc::st_async4(mx_peer + (uint32_t)bb * kHeads * 4u, mloc, bb ? mf1 : mf0);
                 if (!(ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.m_full[bb], ph, abort)))) break;
                 const float mb = fmaxf(mloc, c.mx[bb][hd]) * scale_log2;  // the same in both CTAs
-                tc::mbar_arrive(&c.adv);  // the exchange warpgroup may now send block g + 2
+                tc::mbar_arrive(&c.adv[bb]);  // the exchange warpgroup may now send block g + 2
                 float factor = 1.0f;
                 if (mb > m_ref + kRescaleLog2) {
                     factor = m_ref == -INFINITY ? 0.0f : ex2(m_ref - mb);
@@ -725,7 +728,7 @@ cudaError_t encode_hot_map(const Dev& d, CUtensorMap* map)
 }
 
 cudaError_t launch_attend(const void* hot_map, const Dev& d, const int32_t* req_ids, int B, const void* q,
-                          const int32_t* slots, void* out, float* lse, float sm_scale, cudaStream_t st)
+                          const int32_t* slots, void* out, float* lse, float sm_scale, int max_sms, cudaStream_t st)
 {
     static const cudaError_t attr = cudaFuncSetAttribute(attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                          (int)kSmemLimit);
@@ -740,7 +743,8 @@ cudaError_t launch_attend(const void* hot_map, const Dev& d, const int32_t* req_
         if (e != cudaSuccess) return e;
     }
     const int units = call_units(d, B);
-    const int clusters = std::max(1, std::min(units, sms / 2));
+    const int use_sms = max_sms > 0 ? std::min(max_sms, sms) : sms;
+    const int clusters = std::max(1, std::min(units, use_sms / 2));
     attend_kernel<<<clusters * 2, kAttnThreads, lay.bytes, st>>>(
         *static_cast<const CUtensorMap*>(hot_map), d, req_ids, static_cast<const uint16_t*>(q), slots,
         static_cast<uint16_t*>(out), lse, sm_scale * 1.4426950408889634f, lay, units);
@@ -771,12 +775,20 @@ extern "C" skv_status skv_attend(skv_ctx* ctx, const int32_t* req_ids_dev, int32
     skv::Dev d = ctx->d;
     d.layer_sel = layer;
     if (e == cudaSuccess)
-        e = skv::launch_attend(&ctx->hot_map, d, req_ids_dev, B, q_dev, slots_dev, out_dev, lse_dev, sm_scale, stream);
+        e = skv::launch_attend(&ctx->hot_map, d, req_ids_dev, B, q_dev, slots_dev, out_dev, lse_dev, sm_scale,
+                               ctx->attend_sms, stream);
     if (prev >= 0 && prev != ctx->cfg.device) cudaSetDevice(prev);
     if (e != cudaSuccess) {
         skv::set_last_error_message((std::string("skv_attend: ") + cudaGetErrorString(e)).c_str());
         return SKV_ERR_CUDA;
     }
+    return SKV_OK;
+}
+
+extern "C" skv_status skv_set_attend_sms(skv_ctx* ctx, int32_t sms)
+{
+    if (!ctx || sms < 0) return SKV_ERR_INVALID_ARG;
+    ctx->attend_sms = sms;
     return SKV_OK;
 }
 

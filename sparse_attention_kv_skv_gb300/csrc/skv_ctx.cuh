@@ -24,6 +24,7 @@ struct skv_ctx {
     int plan_resident = 1;  // fused-kernel CTAs resident at once (L2 prefetch budget)
     CUtensorMap hot_map{};  // TMA view of the hot buffer for the attention consumer (built on first use)
     bool hot_map_ready = false;
+    int attend_sms = 0;     // SMs the attention kernel may occupy (0: all)
 };
 
 namespace skv {

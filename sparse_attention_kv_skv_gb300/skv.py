@@ -72,6 +72,7 @@ def _load():
         "skv_get_clock": [vp, P(ctypes.c_uint32), vp],
         "skv_get_stats": [vp, P(ctypes.c_uint64), P(ctypes.c_uint64), P(ctypes.c_uint64), vp],
         "skv_set_gather_events": [vp, vp, vp],
+        "skv_set_attend_sms": [vp, i32],
         "skv_selftest_mma": [vp, vp, vp, i32, i32, i32, vp],
         "skv_attend": [vp, vp, i32, i32, vp, vp, vp, vp, ctypes.c_float, vp],
     }
@@ -107,6 +108,7 @@ skv_export_hot = lib.skv_export_hot
 skv_get_clock = lib.skv_get_clock
 skv_get_stats = lib.skv_get_stats
 skv_set_gather_events = lib.skv_set_gather_events
+skv_set_attend_sms = lib.skv_set_attend_sms
 skv_selftest_mma = lib.skv_selftest_mma
 skv_attend = lib.skv_attend
 skv_last_cuda_error = lib.skv_last_cuda_error
@@ -286,6 +288,10 @@ class Context:
         check(skv_get_stats(self.h, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c), _stream_handle(stream)),
               "skv_get_stats")
         return {"calls": a.value, "hits": b.value, "misses": c.value}
+
+    def set_attend_sms(self, sms: int = 0) -> None:
+        """At most `sms` SMs for later attend() calls (0: all; see skv_set_attend_sms)."""
+        check(skv_set_attend_sms(self.h, sms), "skv_set_attend_sms")
 
     def set_gather_events(self, before=None, after=None) -> None:
         check(skv_set_gather_events(self.h, before.cuda_event if before is not None else None,

@@ -47,8 +47,9 @@ def _check_units(p, units, slots, q, out, lse, scale):
         assert np.all(diff <= LSE_ATOL), f"unit {(b, l)}: lse"
 
 
-@pytest.mark.parametrize("scale", [1.0 / 24.0, 0.35])
-def test_attention_over_assembled_slots(scale):
+@pytest.mark.parametrize("scale,sms", [(1.0 / 24.0, 0), (0.35, 0), (0.35, 4)])
+def test_attention_over_assembled_slots(scale, sms):
+    """sms = 4: two clusters walk the six units, three each (cross-unit pipeline)."""
     w = wl.Workload("attn", B=3, L=2, ctx=3000, k=300, S=512, steps=3, fresh=0.3, order=wl.ORDER_SHUFFLED,
                     n_pad=7)
     p = Pair(w, req_perm=[2, 0, 1])
@@ -60,6 +61,7 @@ def test_attention_over_assembled_slots(scale):
         q_d = torch.from_numpy(q).cuda()
         out_d = torch.full((len(units), 128, 512), 0x7FC0, dtype=torch.int16, device="cuda")
         lse_d = torch.full((len(units), 128), float("nan"), device="cuda")
+        p.ctx.set_attend_sms(sms)
         p.ctx.attend(p.req_dev, q_d, p.slots_dev, out_d, lse_d, sm_scale=scale)
         slots = p.slots_dev.cpu().numpy().reshape(len(units), w.k)
         _check_units(p, units, slots, q, out_d.cpu().numpy().view(np.uint16), lse_d.cpu().numpy(), scale)
@@ -152,5 +154,43 @@ def test_attention_full_size_sampled():
         lse = lse_d.cpu().numpy()[pick]
         _check_units(p, [units[n] for n in pick], slots, q[pick], out, lse, scale)
         assert np.isfinite(lse_d.cpu().numpy()).all()  # every unit of the call produced a result
+    finally:
+        p.close()
+
+
+def test_attention_beside_layer_assembly_on_another_stream():
+    """Layer l's attention (limited to 8 SMs: four clusters walking 16 units each) runs on
+    its own stream while layer l + 1 is assembled on another, as a pipelined decode step
+    does; every unit is checked against the definition, and no wait may give up."""
+    w = wl.Workload("attn_pipe", B=64, L=3, ctx=3000, k=320, S=512, steps=3, fresh=0.3)
+    p = Pair(w)
+    side = torch.cuda.Stream()
+    try:
+        for s in range(w.steps - 1):
+            p.step(s)
+        topk = p.gen.step(w.steps - 1, p.lens)
+        rows = [torch.from_numpy(np.ascontiguousarray(topk[:, l, :])).cuda() for l in range(w.L)]
+        slots_l = [torch.empty((w.B, w.k), dtype=torch.int32, device="cuda") for _ in range(w.L)]
+        hm = torch.empty((w.L, w.B), dtype=torch.int32, device="cuda")
+        q = np.stack([_queries(w, [(b, l) for b in range(w.B)]) for l in range(w.L)])
+        q_d = torch.from_numpy(q).cuda()
+        out_d = torch.empty((w.L, w.B, 128, 512), dtype=torch.int16, device="cuda")
+        lse_d = torch.empty((w.L, w.B, 128), device="cuda")
+        p.ctx.set_attend_sms(8)
+        main = torch.cuda.current_stream()
+        done = [torch.cuda.Event() for _ in range(w.L)]
+        for l in range(w.L):
+            p.ctx.assemble_layer(l, p.req_dev, rows[l], slots_l[l], hm[l], hm[l].clone(), stream=main.cuda_stream)
+            done[l].record(main)
+            side.wait_event(done[l])
+            p.ctx.attend(p.req_dev, q_d[l], slots_l[l], out_d[l], lse_d[l], layer=l, sm_scale=0.3,
+                         stream=side.cuda_stream)
+        torch.cuda.synchronize()
+        assert p.ctx.get_device_error() == 0
+        for l in range(w.L):
+            e, o_slots, _, _ = p.orc.assemble_layer(l, p.req_ids, topk[:, l, :].copy())
+            assert e == 0 and np.array_equal(slots_l[l].cpu().numpy(), o_slots)
+            _check_units(p, [(b, l) for b in range(w.B)], o_slots, q[l], out_d[l].cpu().numpy().view(np.uint16),
+                         lse_d[l].cpu().numpy(), 0.3)
     finally:
         p.close()
