@@ -99,11 +99,12 @@ def test_attention_one_layer_and_fully_masked_units():
         p.close()
 
 
-@pytest.mark.parametrize("k", [20, 40])
-def test_attention_short_topk_and_non_request(k):
-    """One and two key blocks (the pipeline never fills), plus an entry whose
-    request id is not a request: zero output and lse = -inf for it."""
-    w = wl.Workload(f"attn_k{k}", B=3, L=2, ctx=700, k=k, S=64, steps=2, fresh=0.5)
+@pytest.mark.parametrize("k,S,ctx", [(20, 64, 700), (40, 64, 700), (4096, 4096, 6000)])
+def test_attention_short_topk_and_non_request(k, S, ctx):
+    """One and two key blocks (the pipeline never fills) and the largest Top-k
+    (k = 4096: 64 blocks), plus an entry whose request id is not a request:
+    zero output and lse = -inf for it."""
+    w = wl.Workload(f"attn_k{k}", B=3, L=2, ctx=ctx, k=k, S=S, steps=2, fresh=0.5)
     p = Pair(w)
     try:
         for s in range(w.steps):
