@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--attend-sms", type=int, default=0,
                     help="with --attend: SMs the attention kernel may occupy (0: all), leaving the rest to the "
                          "assembly running beside it (--pipeline)")
+    ap.add_argument("--prefetch", type=int, default=0,
+                    help="before each assemble call, prefetch each request's N newest tokens (skv_prefetch_recent)")
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--cpu-sample-requests", type=int, default=32)
     ap.add_argument("--cpu-sample-steps", type=int, default=24)
@@ -333,6 +335,10 @@ def run_ours(args):
     slots = torch.empty((w.L, w.B, w.k) if layered else (w.B, w.L, w.k), dtype=torch.int32, device=dev)
     hits = torch.empty((n_dev, w.L, w.B) if layered else (n_dev, w.B, w.L), dtype=torch.int32, device=dev)
     misses = torch.empty_like(hits)
+    pf = args.prefetch
+    if not 0 <= pf <= w.k:
+        raise SystemExit(f"--prefetch must be in [0, {w.k}]")
+    pf_hits, pf_misses = (torch.zeros_like(hits), torch.zeros_like(hits))
     stream = torch.cuda.Stream(device=dev)
     attn_on = args.attend or args.pipeline
     if args.pipeline and not layered:
@@ -372,6 +378,9 @@ def run_ours(args):
         if layered:
             for l in range(w.L):
                 e = s * w.L + l
+                if pf:
+                    ctx.prefetch_recent(req, pf, layer=l, hits=pf_hits[s, l], misses=pf_misses[s, l],
+                                        stream=stream.cuda_stream)
                 ctx.set_gather_events(ev_b[e], ev_a[e])
                 ctx.assemble_layer(l, req, topk_all[s, l], slots[l], hits[s, l], misses[s, l],
                                    stream=stream.cuda_stream)
@@ -385,6 +394,8 @@ def run_ours(args):
                 ev_join.record(side)
                 stream.wait_event(ev_join)
         else:
+            if pf:
+                ctx.prefetch_recent(req, pf, hits=pf_hits[s], misses=pf_misses[s], stream=stream.cuda_stream)
             ctx.set_gather_events(ev_b[s], ev_a[s])
             ctx.assemble(req, topk_all[s], slots, hits[s], misses[s], stream=stream.cuda_stream)
             if attn_on:
@@ -438,18 +449,23 @@ def run_ours(args):
     M = st1["misses"] - st0["misses"]
     H = st1["hits"] - st0["hits"]
     dev_err = ctx.get_device_error()
-    assert st1["calls"] - st0["calls"] == K * per_call and dev_err == 0, \
-        f"{st1['calls'] - st0['calls']} of {K * per_call} timed calls succeeded; device error bits {dev_err}"
+    calls = K * per_call * (2 if pf else 1)  # a prefetch is an assemble call of its own
+    assert st1["calls"] - st0["calls"] == calls and dev_err == 0, \
+        f"{st1['calls'] - st0['calls']} of {calls} timed calls succeeded; device error bits {dev_err}"
     gather_s = sum(event_ms(ev_b[e], ev_a[e]) for e in range(W * per_call, n_dev * per_call)) / 1e3
     per_step_m = misses[W:].sum(dim=(1, 2)).cpu().numpy().astype(np.int64)
     per_step_h = hits[W:].sum(dim=(1, 2)).cpu().numpy().astype(np.int64)
-    assert int(per_step_m.sum()) == M
-    tokens = float(H + M)
+    pf_m = pf_misses[W:].sum(dim=(1, 2)).cpu().numpy().astype(np.int64)
+    pf_h = pf_hits[W:].sum(dim=(1, 2)).cpu().numpy().astype(np.int64)
+    assert int(per_step_m.sum() + pf_m.sum()) == M and int(per_step_h.sum() + pf_h.sum()) == H
+    M_step = int(per_step_m.sum())  # rows the assemble calls moved (the prefetches moved the rest of M)
+    tokens = float(per_step_h.sum() + M_step)  # Top-k entries assembled
 
     # step roofline: slower of link and HBM terms, per step
     t_roof = 0.0
-    for m_s, h_s in zip(per_step_m, per_step_h):
-        t_roof += max(m_s * rb / (link["h2d"] * 1e9), hbm_algorithmic_bytes(w, int(m_s), int(h_s)) / (hbm_peak * 1e9))
+    for m_s, h_s, pm, ph in zip(per_step_m, per_step_h, pf_m, pf_h):
+        hbm = hbm_algorithmic_bytes(w, int(m_s), int(h_s)) + (hbm_algorithmic_bytes(w, int(pm), int(ph)) if pf else 0)
+        t_roof += max((m_s + pm) * rb / (link["h2d"] * 1e9), hbm / (hbm_peak * 1e9))
 
     attention = None
     if attn_on:
@@ -500,8 +516,14 @@ def run_ours(args):
         gbs, tps, info = cpu_baseline(w, pool, args.cpu_sample_requests, args.cpu_sample_steps)
         cpu = {"value": gbs, "unit": "GB/s", "cores": info["cores"], "kind": "oracle", "sample": info["sample"],
                "assembled_tokens_per_s": tps}
+    prefetch = None
+    if pf:
+        prefetch = {"entry_point": "skv_prefetch_recent (before every assemble call, same stream)", "window": pf,
+                    "prefetched_rows_per_step": float(pf_m.sum()) / K,
+                    "step_missed_rows_per_step": M_step / K,
+                    "step_miss_rate": M_step / max(tokens, 1.0)}
     if rank == 0:
-        achieved = M * rb / gather_s / 1e9
+        achieved = M_step * rb / gather_s / 1e9
         kname = "plan_kernel<fused> (sparse diff + LRU + gather)"
         out = {
             "metric": METRIC,
@@ -521,11 +543,12 @@ def run_ours(args):
                        "write_back_per_step": w.appends, "cuda_graph": use_graph,
                        "layered": layered, "turn_every": w.turn_every, "turn_tokens": w.turn_tokens,
                        "attend": attn_on, "pipeline": bool(args.pipeline), "attend_sms": args.attend_sms,
+                       "prefetch_window": pf,
                        "l2": "inputs larger than L2: each step writes the missed rows (~0.6 GB) into a "
                              f"{w.hot_bytes() / 1e9:.2f} GB hot buffer and reads {w.B * w.L * w.max_context * 4 / 1e6:.0f} MB "
                              "of token->slot maps; no flush"},
             "assembled_tokens_per_s": tokens_all / elapsed_max,
-            "miss_rate": M / max(tokens, 1.0),
+            "miss_rate": M_step / max(tokens, 1.0),
             "missed_rows_per_step": M / K,
             "step_roofline_frac": t_roof / elapsed,
             "roofline": {"bound": "host_link", "kernel": kname,
@@ -534,7 +557,7 @@ def run_ours(args):
                          "traffic": profiled_traffic(w),
                          "traffic_source": "dram read+write of one c2 step captured with ncu, scaled by units "
                                            f"({PROFILED_TRAFFIC['summary']}); host-link reads = 1152 B per missed row",
-                         "link_bytes_per_step": M * rb / K,
+                         "link_bytes_per_step": M_step * rb / K,
                          "peak_source": "pinned cudaMemcpyAsync host->device, 1 GiB, best of 10, this run",
                          "kernel_share_of_step": gather_s / elapsed,
                          "hbm": {"peak": hbm_peak, "peak_source": hbm_src,
@@ -544,9 +567,10 @@ def run_ours(args):
                           "gbs": warm[0][1] * rb / warm[0][0] / 1e6} if rank == 0 else None,
             "warmup_steps_ms": [round(t, 3) for t, _ in warm],
             "attention": attention,
+            "prefetch": prefetch,
             "link_gbs": link,
             "e2e": e2e,
-            "gpu_launches": K * (2 * per_call + (per_call if attn_on else 0) + (2 if w.appends else 0))
+            "gpu_launches": K * ((5 if pf else 2) * per_call + (per_call if attn_on else 0) + (2 if w.appends else 0))
                             + sum(2 * w.B for s in range(W, n_dev) if new_turn(s)),
             "clocks": clocks,
             "cpu_baseline": cpu,

@@ -205,6 +205,37 @@ SKV_API skv_status skv_assemble_layer(skv_ctx *ctx, const int32_t *req_ids_dev, 
                                       const int32_t *topk_dev, int32_t *slots_dev, int32_t *hits_dev,
                                       int32_t *misses_dev, skv_stream_t stream);
 
+/* Prefetch: bring tokens that a coming step is expected to select into the
+ * hot buffers ahead of that step, so that its assemble finds them resident
+ * and moves fewer rows over the host link while the attention waits (the
+ * pages: XM-Sparse keeps HiSparse's prefetching -- "XM-Sparse: Netpreme X-Mem
+ * ...", section "与SGLang HiSparse的集成"; the overhead of on-demand data
+ * movement -- "Sparse Attention-Driven KVCache Management for Domestic AI
+ * Supernodes", agenda item 3).  A prefetch IS an assemble of the candidate
+ * tokens whose slot tensor is not returned: the same validation (ids, range,
+ * no repeats), the same LRU rule, the same gather, the same clock tick, so a
+ * prefetched token counts as used at the prefetch and is the last to be
+ * evicted, and the next assemble that selects it is a hit.
+ *   layer: -1 for every layer (cand_dev [B][L][k]) or one layer in [0, L)
+ *          (cand_dev [B][k]); -1 entries pad a row.
+ *   hits_dev / misses_dev: the counts ([B][L] or [B]), or NULL to discard
+ *          them; misses are the rows the prefetch moved.
+ * The slot tensor goes to scratch owned by the context, so calls on one
+ * context must be ordered (as for every call).  Errors as skv_assemble;
+ * captures into a CUDA graph. */
+SKV_API skv_status skv_prefetch(skv_ctx *ctx, const int32_t *req_ids_dev, int32_t B, int32_t layer,
+                                const int32_t *cand_dev, int32_t *hits_dev, int32_t *misses_dev, skv_stream_t stream);
+
+/* skv_prefetch with a built-in predictor, the recency window: the candidates
+ * of request req_ids_dev[b] are its n newest tokens, [len - n, len) (all of
+ * [0, len) when len < n), for every layer of the call, with len read on the
+ * device when the call runs (after earlier write backs and extends on the
+ * stream).  Decode-time Top-k favours recent tokens; keeping the window
+ * resident turns those picks into hits.  0 <= n <= k, else
+ * SKV_ERR_INVALID_ARG.  Candidates go to scratch owned by the context. */
+SKV_API skv_status skv_prefetch_recent(skv_ctx *ctx, const int32_t *req_ids_dev, int32_t B, int32_t layer, int32_t n,
+                                       int32_t *hits_dev, int32_t *misses_dev, skv_stream_t stream);
+
 /* skv_assemble for callers whose per-step tensors live in host memory
  * (pinned or pageable): copies req_ids [B] and topk [B][L][k] to device
  * staging buffers owned by the context, runs skv_assemble, copies slots, hits

@@ -171,6 +171,42 @@ class Oracle:
                                           _ptr(misses), nthreads)
         return int(err), slots, hits, misses
 
+    def prefetch(self, req_ids, cand: np.ndarray, layer: int = -1, nthreads: int = 1):
+        """Prefetch of candidate tokens -- HiSparse's prefetching, kept by XM-Sparse
+        ("XM-Sparse: Netpreme X-Mem ...", section on the SGLang HiSparse
+        integration).  The pages say no more than that it exists; read plainly, a
+        prefetch makes tokens resident before the step that selects them, which in
+        this model is exactly an assemble of those tokens (same checks, LRU rule,
+        gather and clock tick) whose slots are not handed out.  cand is [B][L][k]
+        (layer -1) or [B][k].  Returns (err, hits, misses)."""
+        if layer < 0:
+            err, _, hits, misses = self.assemble(req_ids, cand, nthreads)
+        else:
+            err, _, hits, misses = self.assemble_layer(layer, req_ids, cand, nthreads)
+        return err, hits, misses
+
+    def recent_candidates(self, req_ids, n: int, layer: int = -1) -> np.ndarray:
+        """The recency-window candidates: for each batch entry, its request's n newest
+        tokens [len - n, len) ascending (all of [0, len) when len < n), -1 padded to
+        k, for every layer ([B][L][k]) or one ([B][k]).  An id that is not an active
+        request gets an all -1 row (the call is rejected for it anyway)."""
+        req = [int(r) for r in req_ids]
+        rows = self.L if layer < 0 else 1
+        out = np.full((len(req), rows, self.k), -1, dtype=np.int32)
+        for b, r in enumerate(req):
+            if not 0 <= r < self.R:
+                continue
+            st = self.export(r, tok2slot=False)
+            if not st["active"]:
+                continue
+            toks = np.arange(max(0, st["len"] - n), st["len"], dtype=np.int32)
+            out[b, :, :toks.size] = toks
+        return out if layer < 0 else out[:, 0, :]
+
+    def prefetch_recent(self, req_ids, n: int, layer: int = -1, nthreads: int = 1):
+        """Prefetch of each request's n newest tokens; returns (err, hits, misses)."""
+        return self.prefetch(req_ids, self.recent_candidates(req_ids, n, layer), layer, nthreads)
+
     def get_error(self) -> int:
         return int(self.lib.orc_get_error(self.h))
 

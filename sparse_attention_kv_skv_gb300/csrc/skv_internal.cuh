@@ -91,5 +91,8 @@ cudaError_t launch_reset_request(const Dev& d, int r, int64_t len, int active, c
 cudaError_t launch_init_lru_all(const Dev& d, cudaStream_t st);
 cudaError_t launch_write_back(const Dev& d, const int32_t* req_ids, int n, const void* rows, cudaStream_t st);
 cudaError_t launch_extend(const Dev& d, int r, int64_t n, const void* rows, cudaStream_t st);
+// Prefetch candidates: per batch entry and layer of the call, the n newest
+// tokens of the request, ascending, -1 padded to k ([B][L or 1][k]).
+cudaError_t launch_recent_candidates(const Dev& d, const int32_t* req_ids, int B, int n, int32_t* cand, cudaStream_t st);
 
 }  // namespace skv

@@ -113,7 +113,34 @@ __global__ void __launch_bounds__(kLifecycleThreads) extend_copy_kernel(Dev d, i
     }
 }
 
+// Candidates of a recency prefetch: for batch entry b (one CTA) and every
+// layer of the call, the n newest tokens of request req_ids[b],
+// [max(0, len - n), len) ascending, then -1 up to k.  The length is read
+// here, on the device, so the window follows write backs and extends earlier
+// on the stream.  An id that is not a request gets an all -1 row (the
+// validation that follows rejects the call for it).
+__global__ void __launch_bounds__(kLifecycleThreads) recent_candidates_kernel(Dev d, const int32_t* __restrict__ req_ids,
+                                                                              int n, int32_t* __restrict__ cand)
+{
+    const int b = blockIdx.x;
+    const int32_t r = req_ids[b];
+    const int64_t len = r >= 0 && r < d.R ? d.len[r] : 0;
+    const int64_t first = len > n ? len - n : 0;
+    const int rows = d.layer_sel >= 0 ? 1 : d.L;
+    int32_t* out = cand + (size_t)b * rows * d.k;
+    for (int i = threadIdx.x; i < rows * d.k; i += blockDim.x) {
+        const int64_t t = first + i % d.k;
+        out[i] = t < len ? (int32_t)t : -1;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_recent_candidates(const Dev& d, const int32_t* req_ids, int B, int n, int32_t* cand, cudaStream_t st)
+{
+    recent_candidates_kernel<<<B, kLifecycleThreads, 0, st>>>(d, req_ids, n, cand);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_extend(const Dev& d, int r, int64_t n, const void* rows, cudaStream_t st)
 {

@@ -309,15 +309,17 @@ skv_status skv_write_back(skv_ctx* ctx, const int32_t* req_ids_dev, int32_t n, c
 
 namespace {
 // The launch sequence of one assemble call over the units described by `d`
-// (all layers, or the one in d.layer_sel).
+// (all layers, or the one in d.layer_sel).  `timed`: record the caller's
+// gather events around the fused kernel (assemble calls only, not prefetches).
 skv_status assemble_impl(skv_ctx* ctx, const Dev& d, const int32_t* req_ids_dev, int32_t B, const int32_t* topk_dev,
-                         int32_t* slots_dev, int32_t* hits_dev, int32_t* misses_dev, cudaStream_t stream)
+                         int32_t* slots_dev, int32_t* hits_dev, int32_t* misses_dev, cudaStream_t stream,
+                         bool timed = true)
 {
     SKV_CUDA(skv::launch_validate(d, req_ids_dev, B, topk_dev, stream));
-    if (ctx->ev_before) SKV_CUDA(record_event(ctx->ev_before, stream));
+    if (timed && ctx->ev_before) SKV_CUDA(record_event(ctx->ev_before, stream));
     SKV_CUDA(skv::launch_plan_gather(d, req_ids_dev, B, topk_dev, slots_dev, hits_dev, misses_dev, ctx->plan_resident,
                                      stream));
-    if (ctx->ev_after) SKV_CUDA(record_event(ctx->ev_after, stream));
+    if (timed && ctx->ev_after) SKV_CUDA(record_event(ctx->ev_after, stream));
     return SKV_OK;
 }
 }  // namespace
@@ -358,6 +360,36 @@ skv_status skv_assemble_layer(skv_ctx* ctx, const int32_t* req_ids_dev, int32_t 
     Dev d = ctx->d;
     d.layer_sel = layer;
     return assemble_impl(ctx, d, req_ids_dev, B, topk_dev, slots_dev, hits_dev, misses_dev, stream);
+}
+
+skv_status skv_prefetch(skv_ctx* ctx, const int32_t* req_ids_dev, int32_t B, int32_t layer, const int32_t* cand_dev,
+                        int32_t* hits_dev, int32_t* misses_dev, skv_stream_t stream)
+{
+    if (!ctx || B < 0 || B > ctx->cfg.max_batch || layer < -1 || layer >= ctx->cfg.num_layers)
+        return SKV_ERR_INVALID_ARG;
+    if (B == 0) return SKV_OK;
+    if (!req_ids_dev || !cand_dev) return SKV_ERR_INVALID_ARG;
+    DeviceGuard g(ctx->cfg.device);
+    Dev d = ctx->d;
+    d.layer_sel = layer;
+    return assemble_impl(ctx, d, req_ids_dev, B, cand_dev, ctx->st_slots, hits_dev ? hits_dev : ctx->st_hits,
+                         misses_dev ? misses_dev : ctx->st_misses, stream, false);
+}
+
+skv_status skv_prefetch_recent(skv_ctx* ctx, const int32_t* req_ids_dev, int32_t B, int32_t layer, int32_t n,
+                               int32_t* hits_dev, int32_t* misses_dev, skv_stream_t stream)
+{
+    if (!ctx || B < 0 || B > ctx->cfg.max_batch || layer < -1 || layer >= ctx->cfg.num_layers || n < 0 ||
+        n > ctx->cfg.topk)
+        return SKV_ERR_INVALID_ARG;
+    if (B == 0) return SKV_OK;
+    if (!req_ids_dev) return SKV_ERR_INVALID_ARG;
+    DeviceGuard g(ctx->cfg.device);
+    Dev d = ctx->d;
+    d.layer_sel = layer;
+    SKV_CUDA(skv::launch_recent_candidates(d, req_ids_dev, B, n, ctx->st_topk, stream));
+    return assemble_impl(ctx, d, req_ids_dev, B, ctx->st_topk, ctx->st_slots, hits_dev ? hits_dev : ctx->st_hits,
+                         misses_dev ? misses_dev : ctx->st_misses, stream, false);
 }
 
 skv_status skv_assemble_host(skv_ctx* ctx, const int32_t* req_ids, int32_t B, const int32_t* topk, int32_t* slots,

@@ -63,6 +63,8 @@ def _load():
         "skv_assemble_host": [vp, vp, i32, vp, vp, vp, vp, vp],
         "skv_assemble_noalloc": [vp, vp, i32, vp, vp, vp, vp, vp],
         "skv_assemble_layer": [vp, vp, i32, i32, vp, vp, vp, vp, vp],
+        "skv_prefetch": [vp, vp, i32, i32, vp, vp, vp, vp],
+        "skv_prefetch_recent": [vp, vp, i32, i32, i32, vp, vp, vp],
         "skv_release": [vp, i32, vp],
         "skv_get_device_error": [vp, P(i32), vp],
         "skv_hot_buffer": [vp, P(vp), P(i64)],
@@ -99,6 +101,8 @@ skv_assemble = lib.skv_assemble
 skv_assemble_host = lib.skv_assemble_host
 skv_assemble_noalloc = lib.skv_assemble_noalloc
 skv_assemble_layer = lib.skv_assemble_layer
+skv_prefetch = lib.skv_prefetch
+skv_prefetch_recent = lib.skv_prefetch_recent
 skv_release = lib.skv_release
 skv_get_device_error = lib.skv_get_device_error
 skv_hot_buffer = lib.skv_hot_buffer
@@ -221,6 +225,21 @@ class Context:
         B = req_ids.numel() if B is None else B
         check(skv_assemble_layer(self.h, _ptr(req_ids), B, layer, _ptr(topk), _ptr(slots), _ptr(hits),
                                  _ptr(misses), _stream_handle(stream)), "skv_assemble_layer")
+
+    def prefetch(self, req_ids, cand, layer: int = -1, hits=None, misses=None, B: int | None = None,
+                 stream=None) -> None:
+        """Assemble of the candidate tokens without a slot tensor: cand is [B][L][k]
+        (layer -1) or [B][k]; hits / misses ([B][L] or [B]) are optional."""
+        B = req_ids.numel() if B is None else B
+        check(skv_prefetch(self.h, _ptr(req_ids), B, layer, _ptr(cand), _ptr(hits), _ptr(misses),
+                           _stream_handle(stream)), "skv_prefetch")
+
+    def prefetch_recent(self, req_ids, n: int, layer: int = -1, hits=None, misses=None, B: int | None = None,
+                        stream=None) -> None:
+        """Prefetch of each request's n newest tokens (every layer, or one)."""
+        B = req_ids.numel() if B is None else B
+        check(skv_prefetch_recent(self.h, _ptr(req_ids), B, layer, n, _ptr(hits), _ptr(misses),
+                                  _stream_handle(stream)), "skv_prefetch_recent")
 
     def assemble_noalloc(self, req_ids, topk, slots, hits, misses, B: int | None = None, stream=None) -> None:
         """skv_assemble with the gather work list in the library's static

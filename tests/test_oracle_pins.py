@@ -52,3 +52,7 @@ def test_layer_calls_match_full_steps():
 
 def test_extend_equals_repeated_write_back():
     pins.check_extend()
+
+
+def test_prefetch_hand_derived():
+    pins.check_prefetch()
