@@ -687,6 +687,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
     tc::fence_before_sync();
     __syncthreads();
     tc::cluster_sync();  // neither CTA leaves while the other may still write into its shared memory
+    if (tid == 0 && *abort) {
+        // A wait of this CTA gave up, so bytes the peer sent before it arrived at the cluster
+        // barrier may still be landing here (nothing waited for them): keep the shared memory
+        // allocated a while longer.
+        for (int i = 0; i < 64; ++i) __nanosleep(1000);
+    }
     if (warp == kMmaWarp) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tbase, kTmemCols);
@@ -727,23 +733,25 @@ cudaError_t encode_hot_map(const Dev& d, CUtensorMap* map)
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-cudaError_t launch_attend(const void* hot_map, const Dev& d, const int32_t* req_ids, int B, const void* q,
-                          const int32_t* slots, void* out, float* lse, float sm_scale, int max_sms, cudaStream_t st)
+cudaError_t prepare_attend(int* device_sms)
 {
-    static const cudaError_t attr = cudaFuncSetAttribute(attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                         (int)kSmemLimit);
-    if (attr != cudaSuccess) return attr;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(device_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)  // a function attribute is per device: set on the device the context lives on
+        e = cudaFuncSetAttribute(attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit);
+    return e;
+}
+
+cudaError_t launch_attend(const void* hot_map, const Dev& d, const int32_t* req_ids, int B, const void* q,
+                          const int32_t* slots, void* out, float* lse, float sm_scale, int max_sms, int device_sms,
+                          cudaStream_t st)
+{
     const AttnLayout lay = attend_layout();
-    if (d.k > (int)kMaxTopk || lay.bytes > kSmemLimit) return cudaErrorInvalidValue;
-    static int sms = 0;  // a persistent grid: one cluster per two SMs (one CTA per SM), at most one per unit
-    if (sms == 0) {
-        int dev = 0;
-        cudaError_t e = cudaGetDevice(&dev);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-    }
+    if (d.k > (int)kMaxTopk || lay.bytes > kSmemLimit || device_sms < 2) return cudaErrorInvalidValue;
+    // a persistent grid: one cluster per two SMs (one CTA per SM), at most one per unit
     const int units = call_units(d, B);
-    const int use_sms = max_sms > 0 ? std::min(max_sms, sms) : sms;
+    const int use_sms = max_sms > 0 ? std::min(max_sms, device_sms) : device_sms;
     const int clusters = std::max(1, std::min(units, use_sms / 2));
     attend_kernel<<<clusters * 2, kAttnThreads, lay.bytes, st>>>(
         *static_cast<const CUtensorMap*>(hot_map), d, req_ids, static_cast<const uint16_t*>(q), slots,
@@ -776,7 +784,7 @@ extern "C" skv_status skv_attend(skv_ctx* ctx, const int32_t* req_ids_dev, int32
     d.layer_sel = layer;
     if (e == cudaSuccess)
         e = skv::launch_attend(&ctx->hot_map, d, req_ids_dev, B, q_dev, slots_dev, out_dev, lse_dev, sm_scale,
-                               ctx->attend_sms, stream);
+                               ctx->attend_sms, ctx->device_sms, stream);
     if (prev >= 0 && prev != ctx->cfg.device) cudaSetDevice(prev);
     if (e != cudaSuccess) {
         skv::set_last_error_message((std::string("skv_attend: ") + cudaGetErrorString(e)).c_str());

@@ -25,6 +25,7 @@ struct skv_ctx {
     CUtensorMap hot_map{};  // TMA view of the hot buffer for the attention consumer (built on first use)
     bool hot_map_ready = false;
     int attend_sms = 0;     // SMs the attention kernel may occupy (0: all)
+    int device_sms = 0;     // SMs of the context's device
 };
 
 namespace skv {

@@ -82,9 +82,12 @@ size_t attend_smem_bytes(int k);
 // launch_attend gathers key rows through.
 cudaError_t encode_hot_map(const Dev& d, struct CUtensorMap_st* map);
 // hot_map: a CUtensorMap over the hot buffer as [R*L*S rows][576] bf16 (box one row x 64, 128B swizzle).
-// max_sms: SMs the kernel may occupy (0: all).
+// max_sms: SMs the kernel may occupy (0: all of device_sms, the device's count).
 cudaError_t launch_attend(const void* hot_map, const Dev& d, const int32_t* req_ids, int B, const void* q,
-                          const int32_t* slots, void* out, float* lse, float sm_scale, int max_sms, cudaStream_t st);
+                          const int32_t* slots, void* out, float* lse, float sm_scale, int max_sms, int device_sms,
+                          cudaStream_t st);
+// Once per context, on its device: the kernel's shared-memory attribute; *device_sms = the SM count.
+cudaError_t prepare_attend(int* device_sms);
 
 // Lifecycle kernels.
 cudaError_t launch_reset_request(const Dev& d, int r, int64_t len, int active, cudaStream_t st);

@@ -236,6 +236,7 @@ skv_status skv_create(const skv_config* cfg, skv_ctx** out)
     SKV_TRY(skv::launch_init_lru_all(d, 0));
     SKV_TRY(skv::prepare_step_kernels(c.topk, c.hot_slots, &x->gather_grid));
     x->plan_resident = skv::plan_resident_ctas(c.topk, c.hot_slots);
+    SKV_TRY(skv::prepare_attend(&x->device_sms));
     SKV_TRY(cudaDeviceSynchronize());
 #undef SKV_TRY
     *out = x;
