@@ -247,6 +247,7 @@ skv_status skv_destroy(skv_ctx* ctx)
 {
     if (!ctx) return SKV_OK;
     DeviceGuard g(ctx->cfg.device);
+    if (!g.ok) return cuda_fail(cudaGetLastError(), "cudaSetDevice");
     cudaDeviceSynchronize();
     free_ctx(ctx);
     return SKV_OK;
@@ -264,6 +265,7 @@ skv_status skv_publish(skv_ctx* ctx, const void* rows, int64_t T, int32_t* out_r
         }
     if (r < 0) return SKV_ERR_NO_FREE_REQUEST;
     DeviceGuard g(ctx->cfg.device);
+    if (!g.ok) return cuda_fail(cudaGetLastError(), "cudaSetDevice");
     const Dev& d = ctx->d;
     const size_t rb = (size_t)d.row_bytes;
     if (rows && T > 0) {
@@ -290,6 +292,7 @@ skv_status skv_release(skv_ctx* ctx, int32_t req, skv_stream_t stream)
     if (!ctx) return SKV_ERR_INVALID_ARG;
     if (req < 0 || req >= ctx->cfg.max_requests || !ctx->active_h[req]) return SKV_ERR_BAD_REQUEST;
     DeviceGuard g(ctx->cfg.device);
+    if (!g.ok) return cuda_fail(cudaGetLastError(), "cudaSetDevice");
     SKV_CUDA(skv::launch_reset_request(ctx->d, req, 0, 0, stream));
     ctx->active_h[req] = 0;
     return SKV_OK;
@@ -302,6 +305,7 @@ skv_status skv_write_back(skv_ctx* ctx, const int32_t* req_ids_dev, int32_t n, c
     if (n == 0) return SKV_OK;
     if (!req_ids_dev || !rows_dev || (reinterpret_cast<uintptr_t>(rows_dev) & 15u)) return SKV_ERR_INVALID_ARG;
     DeviceGuard g(ctx->cfg.device);
+    if (!g.ok) return cuda_fail(cudaGetLastError(), "cudaSetDevice");
     SKV_CUDA(skv::launch_write_back(ctx->d, req_ids_dev, n, rows_dev, stream));
     return SKV_OK;
 }
@@ -335,6 +339,7 @@ skv_status skv_extend(skv_ctx* ctx, int32_t req, const void* rows, int64_t n, sk
     if (!rows || (reinterpret_cast<uintptr_t>(rows) & 15u)) return SKV_ERR_INVALID_ARG;
     if (n > ctx->cfg.max_context) return SKV_ERR_CONTEXT_FULL;
     DeviceGuard g(ctx->cfg.device);
+    if (!g.ok) return cuda_fail(cudaGetLastError(), "cudaSetDevice");
     SKV_CUDA(skv::launch_extend(ctx->d, req, n, rows, stream));
     return SKV_OK;
 }
@@ -346,6 +351,7 @@ skv_status skv_assemble(skv_ctx* ctx, const int32_t* req_ids_dev, int32_t B, con
     if (B == 0) return SKV_OK;
     if (!req_ids_dev || !topk_dev || !slots_dev || !hits_dev || !misses_dev) return SKV_ERR_INVALID_ARG;
     DeviceGuard g(ctx->cfg.device);
+    if (!g.ok) return cuda_fail(cudaGetLastError(), "cudaSetDevice");
     return assemble_impl(ctx, ctx->d, req_ids_dev, B, topk_dev, slots_dev, hits_dev, misses_dev, stream);
 }
 
@@ -358,6 +364,7 @@ skv_status skv_assemble_layer(skv_ctx* ctx, const int32_t* req_ids_dev, int32_t 
     if (B == 0) return SKV_OK;
     if (!req_ids_dev || !topk_dev || !slots_dev || !hits_dev || !misses_dev) return SKV_ERR_INVALID_ARG;
     DeviceGuard g(ctx->cfg.device);
+    if (!g.ok) return cuda_fail(cudaGetLastError(), "cudaSetDevice");
     Dev d = ctx->d;
     d.layer_sel = layer;
     return assemble_impl(ctx, d, req_ids_dev, B, topk_dev, slots_dev, hits_dev, misses_dev, stream);
@@ -371,6 +378,7 @@ skv_status skv_prefetch(skv_ctx* ctx, const int32_t* req_ids_dev, int32_t B, int
     if (B == 0) return SKV_OK;
     if (!req_ids_dev || !cand_dev) return SKV_ERR_INVALID_ARG;
     DeviceGuard g(ctx->cfg.device);
+    if (!g.ok) return cuda_fail(cudaGetLastError(), "cudaSetDevice");
     Dev d = ctx->d;
     d.layer_sel = layer;
     return assemble_impl(ctx, d, req_ids_dev, B, cand_dev, ctx->st_slots, hits_dev ? hits_dev : ctx->st_hits,
@@ -386,6 +394,7 @@ skv_status skv_prefetch_recent(skv_ctx* ctx, const int32_t* req_ids_dev, int32_t
     if (B == 0) return SKV_OK;
     if (!req_ids_dev) return SKV_ERR_INVALID_ARG;
     DeviceGuard g(ctx->cfg.device);
+    if (!g.ok) return cuda_fail(cudaGetLastError(), "cudaSetDevice");
     Dev d = ctx->d;
     d.layer_sel = layer;
     SKV_CUDA(skv::launch_recent_candidates(d, req_ids_dev, B, n, ctx->st_topk, stream));
@@ -400,6 +409,7 @@ skv_status skv_assemble_host(skv_ctx* ctx, const int32_t* req_ids, int32_t B, co
     if (B == 0) return SKV_OK;
     if (!req_ids || !topk || !slots || !hits || !misses) return SKV_ERR_INVALID_ARG;
     DeviceGuard g(ctx->cfg.device);
+    if (!g.ok) return cuda_fail(cudaGetLastError(), "cudaSetDevice");
     const size_t units = (size_t)B * ctx->cfg.num_layers;
     const size_t entries = units * ctx->cfg.topk;
     SKV_CUDA(cudaMemcpyAsync(ctx->st_req, req_ids, (size_t)B * 4, cudaMemcpyHostToDevice, stream));
@@ -417,6 +427,7 @@ skv_status skv_get_device_error(skv_ctx* ctx, int32_t* bits, skv_stream_t stream
 {
     if (!ctx || !bits) return SKV_ERR_INVALID_ARG;
     DeviceGuard g(ctx->cfg.device);
+    if (!g.ok) return cuda_fail(cudaGetLastError(), "cudaSetDevice");
     SKV_CUDA(cudaMemcpyAsync(ctx->host_word, ctx->d.ctl + skv::CTL_ERR, 4, cudaMemcpyDeviceToHost, stream));
     SKV_CUDA(cudaMemsetAsync(ctx->d.ctl + skv::CTL_ERR, 0, 4, stream));
     SKV_CUDA(cudaStreamSynchronize(stream));
@@ -445,6 +456,7 @@ skv_status skv_export_state(skv_ctx* ctx, int32_t req, int32_t* slot2tok, uint32
     if (!ctx) return SKV_ERR_INVALID_ARG;
     if (req < 0 || req >= ctx->cfg.max_requests) return SKV_ERR_BAD_REQUEST;
     DeviceGuard g(ctx->cfg.device);
+    if (!g.ok) return cuda_fail(cudaGetLastError(), "cudaSetDevice");
     const Dev& d = ctx->d;
     const size_t u0 = (size_t)req * d.L;
     const size_t ns = (size_t)d.L * d.S;
@@ -468,6 +480,7 @@ skv_status skv_export_hot(skv_ctx* ctx, int32_t req, void* host_dst, skv_stream_
     if (!ctx || !host_dst) return SKV_ERR_INVALID_ARG;
     if (req < 0 || req >= ctx->cfg.max_requests) return SKV_ERR_BAD_REQUEST;
     DeviceGuard g(ctx->cfg.device);
+    if (!g.ok) return cuda_fail(cudaGetLastError(), "cudaSetDevice");
     const Dev& d = ctx->d;
     SKV_CUDA(cudaStreamSynchronize(stream));
     SKV_CUDA(cudaMemcpy(host_dst, d.hot + (size_t)req * d.L * d.S * d.row_bytes, (size_t)d.L * d.S * d.row_bytes,
@@ -479,6 +492,7 @@ skv_status skv_get_clock(skv_ctx* ctx, uint32_t* clock, skv_stream_t stream)
 {
     if (!ctx || !clock) return SKV_ERR_INVALID_ARG;
     DeviceGuard g(ctx->cfg.device);
+    if (!g.ok) return cuda_fail(cudaGetLastError(), "cudaSetDevice");
     SKV_CUDA(cudaStreamSynchronize(stream));
     SKV_CUDA(cudaMemcpy(clock, ctx->d.ctl + skv::CTL_CLOCK, 4, cudaMemcpyDeviceToHost));
     return SKV_OK;
@@ -488,6 +502,7 @@ skv_status skv_get_stats(skv_ctx* ctx, uint64_t* calls, uint64_t* hits, uint64_t
 {
     if (!ctx) return SKV_ERR_INVALID_ARG;
     DeviceGuard g(ctx->cfg.device);
+    if (!g.ok) return cuda_fail(cudaGetLastError(), "cudaSetDevice");
     unsigned long long st[skv::STAT_WORDS];
     SKV_CUDA(cudaStreamSynchronize(stream));
     SKV_CUDA(cudaMemcpy(st, ctx->d.stats, sizeof(st), cudaMemcpyDeviceToHost));
