@@ -577,10 +577,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
                     sv[4 * m + 3] = cur[4 * m + 3] + pr.w;
                 }
                 const int32_t sp_next = i + 1 < nblk ? slot_of(i + 1) : -1;  // in flight while this block runs
-                if (g + 1 < gtot) {  // S of the next block, possibly of the next unit
-                    if (tid == 0) tc::mbar_arrive_expect_tx(&c.x_full[bb ^ 1], kXBytes);
-                    if (!(ok = own(g + 1, cur))) break;
-                }
+                if (g + 1 < gtot && tid == 0) tc::mbar_arrive_expect_tx(&c.x_full[bb ^ 1], kXBytes);
                 const uint32_t vm = __ballot_sync(0xFFFFFFFFu, sp >= 0 && sp < S);
                 if (vm != 0xFFFFFFFFu) {
 #pragma unroll
@@ -653,12 +650,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
                 else
                     tc::mbar_arrive(&c.p_full[bb]);
                 sp = sp_next;
+                // S of the next block of this unit, read once P(g) is out: its product ran while this
+                // block's softmax did, and the product after it is issued behind O += P(g) V(g), so it
+                // does not delay the release of this block's key stage.  The next unit's first S waits
+                // for that unit's Q, so it is read after this unit's epilogue instead.
+                if (g + 1 < gtot && i + 1 < nblk && !(ok = own(g + 1, cur))) break;
             }
             const int gl = g0 + nblk - 1;  // the unit's last block
-            if (ok) ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.pv_done[gl & 1], ((gl >> 1) & 1), abort));
-            // the denominator: CTA 0's share + CTA 1's share, in that order on both CTAs
+            // the denominator: CTA 0's share + CTA 1's share, in that order on both CTAs (sent
+            // before waiting for the last O += P V, so the two waits overlap)
             if (tid == 0) tc::mbar_arrive_expect_tx(&c.l_full, kHeads * 4u);
             tc::st_async4(lx_peer, l_run, lf_peer);
+            if (ok) ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.pv_done[gl & 1], ((gl >> 1) & 1), abort));
             if (ok) ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.l_full, (uint32_t)n & 1u, abort));
             if (ok) {
                 const float l_all = h == 0 ? l_run + c.lx[hd] : c.lx[hd] + l_run;
@@ -679,6 +682,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
                 tc::fence_before_sync();
                 tc::mbar_arrive(&c.o_free);  // the next unit's first O += P V may overwrite the accumulator
             }
+            if (ok && gl + 1 < gtot) ok = own(gl + 1, cur);  // the first S of the next unit
             g0 += nblk;
             ++n;
         }
