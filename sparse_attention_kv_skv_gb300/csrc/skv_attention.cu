@@ -240,6 +240,22 @@ static_assert(sizeof(AttnCtl) % 16 == 0, "control block alignment");
 // has aborted.  (A cluster-scope acquire here would cost several hundred
 // cycles per wait; the peer's data arrives as transaction bytes on the local
 // barrier, which a CTA-scope acquire observes.)
+// The 18 MMAs of S = Q K^T for CTA rank H: step st covers window dims
+// e = 32H + 16st, in 64-dim box e / 64 at byte (e % 64) * 2 of the swizzled
+// row.  The step's descriptor is the stage's plus that offset in 16-byte units
+// (the address field cannot carry: every stage address is below 2^18).
+template <int H>
+__device__ __forceinline__ void issue_scores(uint32_t tbase, uint64_t dk, uint32_t idesc)
+{
+#pragma unroll
+    for (int st = 0; st < kQKHalf / 16; ++st) {
+        constexpr uint32_t e0 = 32u * H;
+        const uint32_t e = e0 + 16u * st;
+        tc::mma_bf16_ta(tbase + kColS, tbase + kColQ + 8u * st, dk + (((e >> 6) * kBoxBytes + (e & 63u) * 2u) >> 4),
+                        idesc, st > 0 ? 1u : 0u);
+    }
+}
+
 __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, const volatile uint32_t* abort)
 {
     const uint32_t a = tc::smem_u32(bar);
@@ -434,13 +450,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
                         const int s = js % nst;
                         tc::fence_after_sync();
                         const uint32_t kst = aK + s * kStageBytes;
-#pragma unroll 2
-                        for (int st = 0; st < kQKHalf / 16; ++st) {
-                            const uint32_t e = 32u * h + 16u * st;  // window dim of this step (score dims start 32 in for h = 1)
-                            tc::mma_bf16_ta(tbase + kColS, tbase + kColQ + 8u * st,
-                                            tc::sw128_kmajor_desc(kst + (e >> 6) * kBoxBytes + (e & 63u) * 2u),
-                                            idesc_s, st > 0 ? 1u : 0u);
-                        }
+                        // fully unrolled per CTA rank, so every step's descriptor is the stage's plus a
+                        // constant (the MMA issue rate, not the tensor pipe, bounded this loop)
+                        const uint64_t dk = tc::sw128_kmajor_desc(kst);
+                        if (h == 0)
+                            issue_scores<0>(tbase, dk, idesc_s);
+                        else
+                            issue_scores<1>(tbase, dk, idesc_s);
                         tc::mma_commit(&c.s_full);
                         ++js;
                         progressed = true;
