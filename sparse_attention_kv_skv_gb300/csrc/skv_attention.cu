@@ -682,16 +682,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
             if (ok) {
                 const float l_all = h == 0 ? l_run + c.lx[hd] : c.lx[hd] + l_run;
                 tc::fence_after_sync();
-                uint16_t* o = out + ((size_t)u * kHeads + hd) * 512 + h * kVHalf;
                 const float inv = l_all > 0.0f ? 1.0f / l_all : 0.0f;
-                for (int c0 = 0; c0 < kVHalf; c0 += 32) {
-                    float ov[32];
-                    tc::tmem_ld32(tl + kColO + c0, ov);
+                // O goes out through shared memory so that every store instruction writes whole rows:
+                // thread hd puts its row (this CTA's 256 value dims as bf16) into a staging area, 128
+                // columns at a time; then the warp stores its 32 rows two at a time, 16 lanes a row.
+                // The staging area of warp w is its 4 KB of each P tile (rows 0-15 in tile 0, 16-31 in
+                // tile 1): bytes no other thread writes before this warp's next P write, since O += P V
+                // of this unit has completed and the peer writes a P tile only after every thread here
+                // has sent it the next block's maxima.  16-byte chunk c of staged row r sits at chunk
+                // position c ^ (r % 16), which keeps both passes free of bank conflicts.
+                uint8_t* stage = sP + 4096u * (uint32_t)warp;
+                uint16_t* orow = out + ((size_t)u * kHeads + (hd & ~31)) * 512 + h * kVHalf;  // the warp's first row
+                uint8_t* mine = stage + (lane >> 4) * kPBytes + (lane & 15) * 256;
+                for (int half = 0; half < 2; ++half) {
 #pragma unroll
-                    for (int cc = 0; cc < 4; ++cc)
-                        *reinterpret_cast<uint4*>(o + c0 + 8 * cc) =
-                            make_uint4(bf2(ov[8 * cc] * inv, ov[8 * cc + 1] * inv), bf2(ov[8 * cc + 2] * inv, ov[8 * cc + 3] * inv),
-                                       bf2(ov[8 * cc + 4] * inv, ov[8 * cc + 5] * inv), bf2(ov[8 * cc + 6] * inv, ov[8 * cc + 7] * inv));
+                    for (int c0 = 0; c0 < 128; c0 += 32) {
+                        float ov[32];
+                        tc::tmem_ld32(tl + kColO + (uint32_t)(half * 128 + c0), ov);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            *reinterpret_cast<uint4*>(mine + (((c0 / 8 + q) ^ (lane & 15)) << 4)) =
+                                make_uint4(bf2(ov[8 * q] * inv, ov[8 * q + 1] * inv), bf2(ov[8 * q + 2] * inv, ov[8 * q + 3] * inv),
+                                           bf2(ov[8 * q + 4] * inv, ov[8 * q + 5] * inv), bf2(ov[8 * q + 6] * inv, ov[8 * q + 7] * inv));
+                    }
+                    __syncwarp();
+#pragma unroll 4
+                    for (int i = 0; i < 16; ++i) {
+                        const int r = 2 * i + (lane >> 4), cc = lane & 15;
+                        const uint4 w = *reinterpret_cast<const uint4*>(stage + (r >> 4) * kPBytes + (r & 15) * 256 +
+                                                                        ((cc ^ (r & 15)) << 4));
+                        *reinterpret_cast<uint4*>(orow + (size_t)r * 512 + half * 128 + cc * 8) = w;
+                    }
+                    __syncwarp();
                 }
                 if (h == 0 && lse)
                     lse[(size_t)u * kHeads + hd] = l_all > 0.0f ? (m_ref + log2f(l_all)) * 0.69314718055994531f : -INFINITY;
