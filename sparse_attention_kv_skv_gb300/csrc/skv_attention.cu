@@ -20,7 +20,8 @@
 // CTA computes a partial S over its 288 dims for all 64 keys.  The scores are
 // then finished as a reduce-scatter through distributed shared memory: CTA h
 // keeps its partial of keys [32h, 32h + 32), sends the peer its partial of the
-// other 32 (st.async, completing on the peer's mbarrier), adds the peer's
+// other 32 (st.async, completing on the peer's mbarrier; each value as the
+// upper 24 bits of its fp32, relative error at most 2^-16), adds the peer's
 // partial of its own keys, and runs the softmax of those 32 keys; the two CTAs
 // swap their row maxima (so both take the same block maximum and keep the same
 // reference) and their halves of P, so each holds the whole P for O += P V over
@@ -166,7 +167,8 @@ static_assert(128 * (kSoftmaxRegs + kXchgRegs + 2 * kServiceRegs) <= 65536 &&
                   32 * (kSoftmaxRegs + kXchgRegs + 2 * kServiceRegs) <= 16384,
               "the register split must fit the launch's registers, also per SM sub-partition");
 constexpr int kGathers = kBlk / 4 * kWinBoxes;           // four-row TMA copies per block (80)
-constexpr uint32_t kXBytes = kHeads * kHalfBlk * 4;      // the peer's partial scores of my keys (fp32): 16384
+constexpr uint32_t kXBytes = kHeads * kHalfBlk * 3;      // the peer's partial scores of my keys (24-bit): 12288
+constexpr int kXChunks = kHalfBlk * 3 / 16;              // 16-byte chunks a head's partial scores take (6)
 constexpr uint32_t kPBytes = kHeads * kBlk * 2;          // a P tile, both CTAs' halves (bf16): 16384
 constexpr uint32_t kBoxBytes = kBlk * 128;               // one column box of a key stage: 64 rows x 128 B
 constexpr uint32_t kStageBytes = kWinBoxes * kBoxBytes;  // 40960
@@ -220,7 +222,7 @@ struct alignas(16) AttnCtl {
     uint64_t adv[2];             // the softmax warpgroup has taken block g's row maxima (adv[g % 2]: a phase
                                  // every second block, so a waiter that falls behind by a block still sees
                                  // its phase -- a parity wait tells only the current and the previous one)
-    uint64_t x_full[2];          // the peer's partial scores of my keys of a block have arrived (16384 bytes)
+    uint64_t x_full[2];          // the peer's partial scores of my keys of a block have arrived (12288 bytes)
     uint64_t m_full[2];          // the peer's row maxima of a block have arrived (512 bytes)
     uint64_t p_full[2];          // a P tile is complete: my half written, the peer's half arrived (8192 bytes)
     uint64_t pv_done[2];         // O += P V of a block has completed
@@ -254,6 +256,25 @@ __device__ __forceinline__ void issue_scores(uint32_t tbase, uint64_t dk, uint32
         tc::mma_bf16_ta(tbase + kColS, tbase + kColQ + 8u * st, dk + (((e >> 6) * kBoxBytes + (e & 63u) * 2u) >> 4),
                         idesc, st > 0 ? 1u : 0u);
     }
+}
+
+// A partial score crosses the CTA pair as the upper 24 bits of its fp32
+// pattern (sign, exponent, 15 mantissa bits), rounded to nearest: relative
+// error at most 2^-16, the range of fp32.  Four scores pack into three words.
+__device__ __forceinline__ uint32_t f24(float x) { return (__float_as_uint(x) + 0x80u) >> 8; }
+__device__ __forceinline__ void pack24(const float* v, uint32_t* w)
+{
+    const uint32_t a = f24(v[0]), b = f24(v[1]), c = f24(v[2]), d = f24(v[3]);
+    w[0] = a | (b << 24);
+    w[1] = (b >> 8) | (c << 16);
+    w[2] = (c >> 16) | (d << 8);
+}
+__device__ __forceinline__ void unpack24(const uint32_t* w, float* v)
+{
+    v[0] = __uint_as_float(w[0] << 8);
+    v[1] = __uint_as_float(((w[0] >> 24) | (w[1] << 8)) << 8);
+    v[2] = __uint_as_float(((w[1] >> 16) | (w[2] << 16)) << 8);
+    v[3] = __uint_as_float(w[2] & 0xFFFFFF00u);
 }
 
 __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, const volatile uint32_t* abort)
@@ -524,9 +545,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
                 tc::mbar_arrive(&c.s_empty);
                 const uint32_t xb = x_peer + (uint32_t)(g & 1) * kXBytes;
                 const uint32_t rb = (g & 1) ? xf1 : xf0;
+                uint32_t w[kXChunks * 4];
 #pragma unroll
-                for (int m = 0; m < kHalfBlk / 4; ++m)
-                    tc::st_async16(xb + 2048u * m, v[4 * m], v[4 * m + 1], v[4 * m + 2], v[4 * m + 3], rb);
+                for (int j = 0; j < kHalfBlk / 4; ++j) pack24(v + 4 * j, w + 3 * j);
+#pragma unroll
+                for (int m = 0; m < kXChunks; ++m)
+                    tc::st_async16u(xb + 2048u * m, make_uint4(w[4 * m], w[4 * m + 1], w[4 * m + 2], w[4 * m + 3]), rb);
             }
             g0 += nblk;
         }
@@ -584,13 +608,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
                 if (!(ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.x_full[bb], ph, abort)))) break;
                 float sv[kHalfBlk];  // mine + the peer's partial: the full scores of my keys
                 const uint8_t* xrow = sX + bb * kXBytes + hd * 16;
+                uint32_t xw[kXChunks * 4];
 #pragma unroll
-                for (int m = 0; m < kHalfBlk / 4; ++m) {
-                    const float4 pr = *reinterpret_cast<const float4*>(xrow + 2048 * m);
-                    sv[4 * m] = cur[4 * m] + pr.x;
-                    sv[4 * m + 1] = cur[4 * m + 1] + pr.y;
-                    sv[4 * m + 2] = cur[4 * m + 2] + pr.z;
-                    sv[4 * m + 3] = cur[4 * m + 3] + pr.w;
+                for (int m = 0; m < kXChunks; ++m) {
+                    const uint4 pr = *reinterpret_cast<const uint4*>(xrow + 2048 * m);
+                    xw[4 * m] = pr.x;
+                    xw[4 * m + 1] = pr.y;
+                    xw[4 * m + 2] = pr.z;
+                    xw[4 * m + 3] = pr.w;
+                }
+#pragma unroll
+                for (int j = 0; j < kHalfBlk / 4; ++j) {
+                    float px[4];
+                    unpack24(xw + 3 * j, px);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sv[4 * j + e] = cur[4 * j + e] + px[e];
                 }
                 const int32_t sp_next = i + 1 < nblk ? slot_of(i + 1) : -1;  // in flight while this block runs
                 if (g + 1 < gtot && tid == 0) tc::mbar_arrive_expect_tx(&c.x_full[bb ^ 1], kXBytes);
