@@ -71,4 +71,8 @@ def test_host_argument_checks_need_no_gpu(lib_path):
         assert skv.skv_create(ctypes.byref(c), ctypes.byref(h)) == skv.SKV_ERR_INVALID_ARG
     assert skv.skv_destroy(None) == skv.SKV_OK
     assert skv.skv_assemble(None, None, 0, None, None, None, None, None) == skv.SKV_ERR_INVALID_ARG
+    assert skv.skv_prefetch(None, None, 1, -1, None, None, None, None) == skv.SKV_ERR_INVALID_ARG
+    assert skv.skv_prefetch_recent(None, None, 1, -1, 4, None, None, None) == skv.SKV_ERR_INVALID_ARG
+    assert skv.skv_attend(None, None, 1, -1, None, None, None, None, 0.1, None) == skv.SKV_ERR_INVALID_ARG
+    assert skv.skv_set_attend_sms(None, 0) == skv.SKV_ERR_INVALID_ARG
     assert skv.skv_status_string(skv.SKV_ERR_CONTEXT_FULL) == b"SKV_ERR_CONTEXT_FULL"

@@ -148,3 +148,31 @@ def test_recency_prefetch_keeps_the_window_resident():
     finally:
         with_pf.close()
         without.close()
+
+
+def test_prefetch_argument_checks():
+    """Host-side checks: a layer outside [-1, L), a window outside [0, k], a
+    missing candidate tensor -- rejected before anything is enqueued."""
+    from sparse_attention_kv_skv_gb300 import skv
+    w = wl.Workload("pf_args", B=2, L=2, ctx=300, k=16, S=32, steps=1)
+    p = Pair(w)
+    try:
+        clock = p.ctx.clock()
+        cand = torch.full((w.B, w.L, w.k), -1, dtype=torch.int32, device="cuda")
+        req = p.req_dev.data_ptr()
+        assert skv.skv_prefetch_recent(p.ctx.h, req, w.B, w.L, 4, None, None, None) == skv.SKV_ERR_INVALID_ARG
+        assert skv.skv_prefetch_recent(p.ctx.h, req, w.B, -2, 4, None, None, None) == skv.SKV_ERR_INVALID_ARG
+        assert skv.skv_prefetch_recent(p.ctx.h, req, w.B, -1, w.k + 1, None, None, None) == skv.SKV_ERR_INVALID_ARG
+        assert skv.skv_prefetch_recent(p.ctx.h, req, w.B, -1, -1, None, None, None) == skv.SKV_ERR_INVALID_ARG
+        assert skv.skv_prefetch_recent(p.ctx.h, req, w.B + 1, -1, 4, None, None, None) == skv.SKV_ERR_INVALID_ARG
+        assert skv.skv_prefetch(p.ctx.h, req, w.B, -1, None, None, None, None) == skv.SKV_ERR_INVALID_ARG
+        assert skv.skv_prefetch(p.ctx.h, req, w.B, w.L, cand.data_ptr(), None, None, None) == skv.SKV_ERR_INVALID_ARG
+        assert skv.skv_prefetch(p.ctx.h, req, 0, -1, cand.data_ptr(), None, None, None) == skv.SKV_OK  # B = 0: no-op
+        assert skv.skv_prefetch_recent(p.ctx.h, req, w.B, -1, 0, None, None, None) == skv.SKV_OK  # empty window
+        torch.cuda.synchronize()
+        assert p.ctx.clock() == clock + 1  # only the empty-window prefetch ran (an all -1 call still ticks)
+        assert p.orc.prefetch_recent(p.req_ids, 0)[0] == 0
+        p.compare_state()
+        assert p.ctx.get_device_error() == 0
+    finally:
+        p.close()
