@@ -14,6 +14,14 @@ host->device and device->host copies inside the timed region.
 
   python bench.py [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
   torchrun --nproc-per-node N bench.py --gpus N ...   (weak scaling: one replica per GPU)
+
+Variants of the step (reported under their own keys, same metric):
+  --layered           one skv_assemble_layer call per layer instead of one call
+  --prefetch N        skv_prefetch_recent of each request's N newest tokens before
+                      each assemble call (``prefetch``: rows it moved, the step's misses)
+  --attend            skv_attend over each step's slots (``attention``: ms, TFLOP/s)
+  --pipeline          with --layered --attend: layer l's attention on its own stream
+                      beside layer l+1's assembly; --attend-sms caps its SMs
 """
 from __future__ import annotations
 
