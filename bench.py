@@ -236,10 +236,12 @@ def hbm_algorithmic_bytes(w: wl.Workload, M: int, hits: int) -> int:
     return (U * w.k * 4 * 3 + U * w.S * 2 * 2 + (hits + M) * 4 + M * 16 + M * wl.ROW_BYTES)
 
 
-def cpu_baseline(w: wl.Workload, pool_addr: int | None, n_req: int, n_steps: int, warm: int = 2):
+def cpu_baseline(w: wl.Workload, pool_addr: int | None, n_req: int, n_steps: int, warm: int = 2,
+                 one_core_steps: int = 0):
     """The oracle as it stands, on this host's cores, over the first n_req
     requests of the workload for n_steps steady-state steps (after `warm`
-    steps, the first of which is cold).  Returns (GB/s, tokens/s, info)."""
+    steps, the first of which is cold); then, if one_core_steps > 0, that many
+    further steps on one core.  Returns (GB/s, tokens/s, info)."""
     import oracle as orc
     n_req = min(n_req, w.B)
     T_max = w.max_context
@@ -270,12 +272,24 @@ def cpu_baseline(w: wl.Workload, pool_addr: int | None, n_req: int, n_steps: int
             tot_t += dt
             tot_m += int(misses.sum())
             tot_tok += int(hits.sum() + misses.sum())
+    one = None
+    if one_core_steps > 0:
+        t1, m1 = 0.0, 0
+        for s in range(warm + n_steps, warm + n_steps + one_core_steps):
+            topk = gen.step(s, lens)
+            t0 = time.perf_counter()
+            e, slots, hits, misses = o.assemble(req, topk, nthreads=1)
+            t1 += time.perf_counter() - t0
+            assert e == 0
+            m1 += int(misses.sum())
+        one = {"value": m1 * rb / t1 / 1e9, "unit": "GB/s", "cores": 1,
+               "sample": f"{one_core_steps} further steps of the same {n_req} requests"}
     o.close()
     gen.close()
     return (tot_m * rb / tot_t / 1e9, tot_tok / tot_t,
             {"cores": threads, "sample": f"{n_req} of {w.B} requests x {w.L} layers, {n_steps} steady-state steps "
                                         f"after {warm} warm-up steps (first cold), {w.name}",
-             "seconds": tot_t})
+             "seconds": tot_t, "one_core": one})
 
 
 # ---------------------------------------------------------------------------
@@ -521,9 +535,9 @@ def run_ours(args):
     elapsed_max, bytes_all, tokens_all = reduce_results(dist, elapsed, float(M * rb), tokens)
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        gbs, tps, info = cpu_baseline(w, pool, args.cpu_sample_requests, args.cpu_sample_steps)
+        gbs, tps, info = cpu_baseline(w, pool, args.cpu_sample_requests, args.cpu_sample_steps, one_core_steps=2)
         cpu = {"value": gbs, "unit": "GB/s", "cores": info["cores"], "kind": "oracle", "sample": info["sample"],
-               "assembled_tokens_per_s": tps}
+               "assembled_tokens_per_s": tps, "one_core": info["one_core"]}
     prefetch = None
     if pf:
         prefetch = {"entry_point": "skv_prefetch_recent (before every assemble call, same stream)", "window": pf,
