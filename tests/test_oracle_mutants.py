@@ -12,6 +12,7 @@ import subprocess
 import sys
 import tempfile
 
+import numpy as np
 import pytest
 
 import oracle as orc
@@ -116,3 +117,35 @@ def test_every_planted_mistake_is_caught():
 
 def test_unmodified_oracle_passes_the_same_checks():
     assert not _caught(orc.build())
+
+
+PREFETCH_MUTANTS = {
+    # the window one token short at its newest end
+    "window_misses_newest": lambda self, req, n, layer=-1: _shift_window(self, req, n, layer, end=-1),
+    # the window one token too long at its oldest end
+    "window_one_older": lambda self, req, n, layer=-1: _shift_window(self, req, n + 1, layer, end=0),
+    # the whole context instead of the newest n tokens
+    "window_from_start": lambda self, req, n, layer=-1: _shift_window(self, req, n, layer, end=0, from_start=True),
+}
+
+
+def _shift_window(o, req_ids, n, layer, end, from_start=False):
+    rows = o.L if layer < 0 else 1
+    out = np.full((len(req_ids), rows, o.k), -1, dtype=np.int32)
+    for b, r in enumerate(req_ids):
+        st = o.export(int(r), tok2slot=False)
+        hi = st["len"] + end
+        lo = 0 if from_start else max(0, hi - n)
+        toks = np.arange(lo, hi, dtype=np.int32)[: o.k]
+        out[b, :, :toks.size] = toks
+    return out if layer < 0 else out[:, 0, :]
+
+
+@pytest.mark.parametrize("name", sorted(PREFETCH_MUTANTS))
+def test_every_planted_prefetch_window_mistake_is_caught(name, monkeypatch):
+    """A wrong recency window in the oracle's prefetch fails the hand-derived prefetch pins."""
+    sys.path.insert(0, HERE)
+    import oracle_pins as pins
+    monkeypatch.setattr(orc.Oracle, "recent_candidates", PREFETCH_MUTANTS[name])
+    with pytest.raises(AssertionError):
+        pins.check_prefetch()
