@@ -49,10 +49,12 @@ _lib = None
 
 
 def lib():
+    """The generator library: the in-place build, or the copy SKV_WORKLOAD_LIB
+    names (the sanitizer test loads an instrumented build that way)."""
     global _lib
     if _lib is None:
-        build()
-        L = ctypes.CDLL(_LIB)
+        path = os.environ.get("SKV_WORKLOAD_LIB") or build()
+        L = ctypes.CDLL(path)
         u8p = ctypes.c_void_p
         L.skvw_splitmix64_at.restype = ctypes.c_uint64
         L.skvw_splitmix64_at.argtypes = [ctypes.c_uint64, ctypes.c_uint64]
