@@ -120,7 +120,11 @@ void host_copy(uint8_t* dst, const uint8_t* src, size_t n)
         const size_t o = (size_t)i * per;
         if (o >= n) break;
         const size_t len = n - o < per ? n - o : per;
-        th.emplace_back([=] { std::memcpy(dst + o, src + o, len); });
+        try {  // no C++ exception may leave a C entry point
+            th.emplace_back([=] { std::memcpy(dst + o, src + o, len); });
+        } catch (...) {  // no thread to spare: copy this share here
+            std::memcpy(dst + o, src + o, len);
+        }
     }
     for (auto& t : th) t.join();
 }
@@ -180,7 +184,12 @@ skv_status skv_create(const skv_config* cfg, skv_ctx** out)
     skv_ctx* x = new (std::nothrow) skv_ctx();
     if (!x) return SKV_ERR_OOM;
     x->cfg = c;
-    x->active_h.assign(c.max_requests, 0);
+    try {  // no C++ exception may leave a C entry point
+        x->active_h.assign(c.max_requests, 0);
+    } catch (const std::bad_alloc&) {
+        delete x;
+        return SKV_ERR_OOM;
+    }
     Dev& d = x->d;
     d.R = c.max_requests;
     d.L = c.num_layers;
@@ -466,7 +475,12 @@ skv_status skv_export_state(skv_ctx* ctx, int32_t req, int32_t* slot2tok, uint32
     if (tok2slot) SKV_CUDA(cudaMemcpy(tok2slot, d.tok2slot + u0 * d.T_max, (size_t)d.L * d.T_max * 4,
                                       cudaMemcpyDeviceToHost));
     if (lru) {
-        std::vector<uint16_t> tmp(ns);
+        std::vector<uint16_t> tmp;
+        try {  // no C++ exception may leave a C entry point
+            tmp.resize(ns);
+        } catch (const std::bad_alloc&) {
+            return SKV_ERR_OOM;
+        }
         SKV_CUDA(cudaMemcpy(tmp.data(), d.lru + u0 * d.S, ns * 2, cudaMemcpyDeviceToHost));
         for (size_t i = 0; i < ns; ++i) lru[i] = tmp[i];
     }
