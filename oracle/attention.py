@@ -14,8 +14,9 @@ only.  For one (request, layer) unit, with q [H][576] (a 512-wide latent plus
 
 in float64, with numpy's matmul as a step.  All masked: out = 0, lse = -inf.
 
-Parity status: pinned by closed forms in tests/test_oracle_attention.py
-(uniform scores, one key, two keys, masking, key order).
+Parity status: pinned in tests/test_oracle_attention.py by closed forms
+(uniform scores, one key, two keys, a repeated key), invariants (masking, key
+order) and a scalar-loop evaluation of the definition on tiny inputs.
 """
 from __future__ import annotations
 
