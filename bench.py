@@ -210,14 +210,13 @@ def hbm_peak_gbs():
     return 6800.0, "fallback 6.8 TB/s"
 
 
-# DRAM traffic of the fused kernel from the ncu capture summarised in
-# profiles/plan_gather_kernel_c2_16k_b64.md (one steady c2 step, 512 units):
+# DRAM traffic of the fused kernel from one ncu capture of a steady step of
+# the 16K-context, batch-64, 8-layer workload (512 units):
 # dram__bytes_read.sum + dram__bytes_write.sum.  Valid only while the kernel
 # source is the one that was captured; scaled to other workloads by units.
 PROFILED_TRAFFIC = {"source": "sparse_attention_kv_skv_gb300/csrc/skv_step_kernels.cu",
                     "sha256": "8d62c9430bfe062f37f24aee3d4a0a50e36097b789fc6c89a43000a43cf221c6",
-                    "units": 512, "dram_bytes": 42.504192e6 + 197.452800e6,
-                    "summary": "profiles/plan_gather_kernel_c2_16k_b64.md"}
+                    "units": 512, "dram_bytes": 42.504192e6 + 197.452800e6}
 
 
 def profiled_traffic(w: wl.Workload):
@@ -577,8 +576,9 @@ def run_ours(args):
                          "achieved": achieved,
                          "peak": link["h2d"], "unit": "GB/s", "frac": achieved / link["h2d"],
                          "traffic": profiled_traffic(w),
-                         "traffic_source": "dram read+write of one c2 step captured with ncu, scaled by units "
-                                           f"({PROFILED_TRAFFIC['summary']}); host-link reads = 1152 B per missed row",
+                         "traffic_source": "dram read+write of one steady step of the 16K-context batch-64 "
+                                           "8-layer workload captured with ncu, scaled by units; host-link reads "
+                                           "= 1152 B per missed row",
                          "link_bytes_per_step": M_step * rb / K,
                          "peak_source": "pinned cudaMemcpyAsync host->device, 1 GiB, best of 10, this run",
                          "kernel_share_of_step": gather_s / elapsed,
