@@ -15,6 +15,14 @@ host->device and device->host copies inside the timed region.
   python bench.py [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
   torchrun --nproc-per-node N bench.py --gpus N ...   (weak scaling: one replica per GPU)
 
+After the headline region (plain step only; ``--extra-steps 0`` skips it) the
+same context runs on: ``attention`` times skv_attend over each further step's
+slots (CUDA events around the call; TFLOP/s against the measured bf16 peaks),
+and ``decode_step`` times the layer-pipelined decode step (per layer
+skv_assemble_layer, then that layer's skv_attend on a second stream limited to
+``--decode-attend-sms`` SMs beside the next layer's assembly; graph replays).
+Neither changes ``value`` or ``ms_per_step``.
+
 Variants of the step (reported under their own keys, same metric):
   --layered           one skv_assemble_layer call per layer instead of one call
   --prefetch N        skv_prefetch_recent of each request's N newest tokens before
@@ -66,6 +74,11 @@ def parse():
     ap.add_argument("--prefetch", type=int, default=0,
                     help="before each assemble call, prefetch each request's N newest tokens (skv_prefetch_recent)")
     ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--extra-steps", type=int, default=12,
+                    help="after the headline region (plain step only): this many steps with skv_attend over each "
+                         "step's slots (`attention`), then as many pipelined decode steps (`decode_step`); 0: none")
+    ap.add_argument("--decode-attend-sms", type=int, default=96,
+                    help="SMs the attention may occupy in the pipelined decode step")
     ap.add_argument("--cpu-sample-requests", type=int, default=32)
     ap.add_argument("--cpu-sample-steps", type=int, default=24)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -291,6 +304,126 @@ def cpu_baseline(w: wl.Workload, pool_addr: int | None, n_req: int, n_steps: int
              "seconds": tot_t, "one_core": one})
 
 
+def tensor_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    peaks = json.load(open(p)) if os.path.exists(p) else {}
+    if "bf16_tflops_sustained" in peaks:
+        return (float(peaks["bf16_tflops_sustained"]), float(peaks.get("bf16_tflops", peaks["bf16_tflops_sustained"])),
+                "MEASURED_PEAKS.json bf16_tflops_sustained / bf16_tflops (measured cuBLAS bf16)")
+    return 1700.0, 1900.0, "fallback 1.7 PFLOP/s sustained, 1.9 PFLOP/s burst"
+
+
+def run_extras(torch, ctx, w: wl.Workload, dev, stream, req, att_topk, dec_topk, attend_sms: int):
+    """Timed after the headline region, on the same context (its state runs
+    on): (1) each of len(att_topk) steps assembles, then runs skv_attend over
+    that step's slots, with CUDA events around the attention call alone (the
+    first two calls are warm-up); (2) the decode step of F1 + F4: per layer,
+    skv_assemble_layer on the main stream and, as soon as it is done, that
+    layer's skv_attend on a second stream limited to `attend_sms` SMs, beside
+    the next layer's assembly; each step one CUDA graph replay, the first two
+    eager (warm-up)."""
+    B, L, k = w.B, w.L, w.k
+    units = B * L
+    flops_per_entry = 2.0 * 128 * (576 + 512)  # q.k over 576 dims and p.v over 512, 128 heads
+    t_sus, t_burst, t_src = tensor_peaks()
+    q_host = np.stack([wl.fill_q(w.base_seed, b, l) for b in range(B) for l in range(L)])
+    q_all = torch.from_numpy(q_host).to(dev).view(torch.int16).view(units, 128, 576)
+    del q_host
+    out = torch.empty((units, 128, 512), dtype=torch.int16, device=dev)
+    lse = torch.empty((units, 128), dtype=torch.float32, device=dev)
+    slots = torch.empty((B, L, k), dtype=torch.int32, device=dev)
+    n_a = len(att_topk)
+    hm = torch.empty((n_a, 2, B, L), dtype=torch.int32, device=dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_a)]
+    ctx.set_attend_sms(0)
+    with torch.cuda.stream(stream):
+        for i, t in enumerate(att_topk):
+            ctx.assemble(req, t, slots, hm[i, 0], hm[i, 1], stream=stream.cuda_stream)
+            ev[i][0].record(stream)
+            ctx.attend(req, q_all, slots, out, lse, stream=stream.cuda_stream)
+            ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    assert ctx.get_device_error() == 0
+    warm = min(2, n_a - 1)
+    ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(warm, n_a)]
+    ent = hm[warm:].sum(dim=(1, 2, 3)).cpu().numpy().astype(np.float64)  # valid entries (hits + misses) per step
+    att_s = sum(ms) / 1e3
+    flops = float(ent.sum()) * flops_per_entry
+    attention = {"kernel": "attend_kernel (tcgen05, clusters of two CTAs)", "calls": len(ms),
+                 "ms_per_call": 1e3 * att_s / len(ms), "ms_min": min(ms), "ms_max": max(ms),
+                 "units_per_call": units, "heads": 128, "dims": 576, "value_dims": 512,
+                 "algorithmic_flops_per_call": flops / len(ms), "tflops": flops / att_s / 1e12,
+                 "frac_of_tensor_peak": flops / att_s / 1e12 / t_sus,
+                 "frac_of_burst_peak": flops / att_s / 1e12 / t_burst,
+                 "tensor_peak_tflops": t_sus, "burst_peak_tflops": t_burst, "tensor_peak_source": t_src,
+                 "key_bytes_per_call": float(ent.sum()) * wl.ROW_BYTES / len(ms),
+                 "key_gbs": float(ent.sum()) * wl.ROW_BYTES / att_s / 1e9,
+                 "timing": "CUDA events around each skv_attend over the slots its step's assemble emitted "
+                           f"({warm} warm-up calls not counted)"}
+
+    # (2) the pipelined decode step
+    n_d = len(dec_topk)
+    q_l = q_all.view(B, L, 128, 576).transpose(0, 1).contiguous()  # [L][B]: a layer call's units are ordered b
+    del q_all
+    out_l = torch.empty((L, B, 128, 512), dtype=torch.int16, device=dev)
+    lse_l = torch.empty((L, B, 128), dtype=torch.float32, device=dev)
+    slots_l = torch.empty((L, B, k), dtype=torch.int32, device=dev)
+    hm_l = torch.empty((n_d, 2, L, B), dtype=torch.int32, device=dev)
+    side = torch.cuda.Stream(device=dev)
+    ev_layer = [torch.cuda.Event() for _ in range(L)]
+    ev_join = torch.cuda.Event()
+    ctx.set_attend_sms(attend_sms)
+
+    def dec_step(i):
+        for l in range(L):
+            ctx.assemble_layer(l, req, dec_topk[i][l], slots_l[l], hm_l[i, 0, l], hm_l[i, 1, l],
+                               stream=stream.cuda_stream)
+            ev_layer[l].record(stream)
+            side.wait_event(ev_layer[l])
+            ctx.attend(req, q_l[l], slots_l[l], out_l[l], lse_l[l], layer=l, stream=side.cuda_stream)
+        ev_join.record(side)
+        stream.wait_event(ev_join)
+
+    warm_d = min(2, n_d - 1)
+    graphs = []
+    with torch.cuda.stream(stream):
+        for i in range(warm_d, n_d):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                dec_step(i)
+            graphs.append(g)
+    torch.cuda.synchronize()
+    st0 = ctx.stats()
+    with torch.cuda.stream(stream):
+        for i in range(warm_d):
+            dec_step(i)
+    torch.cuda.synchronize()
+    st1 = ctx.stats()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for g in graphs:
+            g.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    st2 = ctx.stats()
+    ctx.set_attend_sms(0)
+    assert ctx.get_device_error() == 0 and st2["calls"] - st1["calls"] == len(graphs) * L
+    dec_s = a.elapsed_time(b) / 1e3
+    n_t = len(graphs)
+    m_rows = st2["misses"] - st1["misses"]
+    entries = float(hm_l[warm_d:].sum().item())
+    decode_step = {"steps": n_t, "ms_per_step": 1e3 * dec_s / n_t, "layers": L, "attend_sms": attend_sms,
+                   "missed_kv_gbs": m_rows * wl.ROW_BYTES / dec_s / 1e9,
+                   "assembled_tokens_per_s": entries / dec_s,
+                   "attention_tflops": entries * flops_per_entry / dec_s / 1e12,
+                   "what": "per layer: skv_assemble_layer on the main stream, then that layer's skv_attend on a "
+                           "second stream (at most attend_sms SMs) beside the next layer's assembly; one CUDA "
+                           f"graph replay per step, {warm_d} eager warm-up steps",
+                   "warmup_calls_ok": st1["calls"] - st0["calls"] == warm_d * L}
+    return attention, decode_step
+
+
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
@@ -336,12 +469,22 @@ def run_ours(args):
                            device=dev)
     wb_rows = None
     host_steps = []
-    for s in range(n_dev + args.e2e_steps):
+    # after the headline region: one attention call per step's slots, then the
+    # decode step (assembly + attention, layer by layer); only for the plain step
+    extras = (args.extra_steps > 0 and not (w.appends or w.turn_every or layered or args.attend or args.pipeline
+                                            or args.prefetch))
+    n_x = args.extra_steps if extras else 0
+    att_topk, dec_topk = [], []
+    for s in range(n_dev + args.e2e_steps + 2 * n_x):
         x = gen.step(s, [w.len_at(s)] * w.B)
         if s < n_dev:
             topk_all[s].copy_(torch.from_numpy(np.ascontiguousarray(x.transpose(1, 0, 2)) if layered else x))
-        else:
+        elif s < n_dev + args.e2e_steps:
             host_steps.append(torch.from_numpy(x).pin_memory())
+        elif s < n_dev + args.e2e_steps + n_x:
+            att_topk.append(torch.from_numpy(x).to(dev))                                   # [B][L][k]
+        else:
+            dec_topk.append(torch.from_numpy(np.ascontiguousarray(x.transpose(1, 0, 2))).to(dev))  # [L][B][k]
     if w.appends:
         # the appended rows' contents do not affect timing: one fixed block per step
         wb_rows = torch.zeros((w.B, w.L, rb), dtype=torch.uint8, device=dev)
@@ -531,6 +674,12 @@ def run_ours(args):
                "ms_per_step": 1e3 * e2e_s / len(host_steps), "steps": len(host_steps),
                "entry_point": "skv_assemble_host (pinned host buffers; copies + sync inside the timed region)"}
 
+    decode_step = None
+    if extras:
+        attention, decode_step = run_extras(torch, ctx, w, dev, stream, req, att_topk, dec_topk,
+                                            args.decode_attend_sms)
+    del att_topk, dec_topk
+
     elapsed_max, bytes_all, tokens_all = reduce_results(dist, elapsed, float(M * rb), tokens)
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -589,6 +738,7 @@ def run_ours(args):
                           "gbs": warm[0][1] * rb / warm[0][0] / 1e6} if rank == 0 else None,
             "warmup_steps_ms": [round(t, 3) for t, _ in warm],
             "attention": attention,
+            "decode_step": decode_step,
             "prefetch": prefetch,
             "link_gbs": link,
             "e2e": e2e,

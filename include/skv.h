@@ -5,19 +5,25 @@
  * of every request in a host memory pool and only a cache of hot tokens on the
  * accelerator; each decode step, per layer, the sparse-attention Top-k indices
  * say which tokens the attention kernel needs, and those tokens are assembled
- * on the device on demand, at token (not page) granularity:
- *   - "Sparse Attention-Driven KVCache Management for Domestic AI Supernodes"
- *     (ml-summit.org talk abstract): abstract, and agenda item 2 (host storage,
- *     device cache and index mapping of the SparseKVCacheManager; the UniDex
- *     index-copy operator that keeps the step graph-executable);
- *   - "SGLang и Tair представили иерархичную Sparse Attention для хранения
- *     полного KV Cache на CPU и экономии GPU-памяти": paragraph 1 (full KV on
- *     the CPU, a Top-k LRU buffer on the GPU), paragraph 3 (incremental
- *     transfer of sparse changes by the Sparse Diff Kernel, fast I/O kernels);
- *   - "XM-Sparse: Netpreme X-Mem 突破稀疏注意力吞吐极限": section "与SGLang
- *     HiSparse的集成" (CUDA Graph support; lifecycle publish, acquire, write
- *     back, release), section "为何稀疏注意力需要快速高容量内存层" (a hot KV
- *     buffer in HBM reduces external-memory reads).
+ * on the device on demand, at token (not page) granularity.  The sources, and
+ * the short tags the "Source:" line of each declaration below uses for them:
+ *   [talk]   "Sparse Attention-Driven KVCache Management for Domestic AI
+ *            Supernodes" (ml-summit.org talk abstract): abstract, and agenda
+ *            item 2 (host storage, device cache and index mapping of the
+ *            SparseKVCacheManager; the UniDex index-copy operator that keeps
+ *            the step graph-executable);
+ *   [digest] "SGLang и Tair представили иерархичную Sparse Attention для
+ *            хранения полного KV Cache на CPU и экономии GPU-памяти":
+ *            paragraph 1 (full KV on the CPU, a Top-k LRU buffer on the GPU),
+ *            paragraph 3 (incremental transfer of sparse changes by the Sparse
+ *            Diff Kernel, fast I/O kernels);
+ *   [xm]     "XM-Sparse: Netpreme X-Mem 突破稀疏注意力吞吐极限": section
+ *            "与SGLang HiSparse的集成" (CUDA Graph support; lifecycle publish,
+ *            acquire, write back, release), section
+ *            "为何稀疏注意力需要快速高容量内存层" (a hot KV buffer in HBM
+ *            reduces external-memory reads).
+ * Where the pages are silent, a declaration's Source line says so and states
+ * the reading this library implements.
  *
  * Geometry.  R request slots, L layers, T_max tokens of pool room per request,
  * rows of row_bytes bytes (576 bf16 = 1152 B for an MLA latent of 512 plus 64
@@ -32,8 +38,8 @@
  *   slot2tok [R][L][S] int32        device; -1 = empty slot
  *   ts       [R][L][S] uint32       device; clock of the step that last used the slot (0 = never)
  *   lru      [R][L][S] uint16       device; the S slots ordered by (ts, slot), least recent first
- *   len/active per request, the step clock, the sticky error word, and the
- *   gather work list [max_batch * L * k] -- all device memory.
+ *   len/active per request, the step clock and the sticky error word -- all
+ *   device memory.
  * No call after skv_create allocates; skv_assemble and skv_write_back are
  * therefore safe to capture in a CUDA graph.
  *
@@ -61,6 +67,18 @@
  * non-zero every later skv_assemble / skv_write_back is a no-op with -1
  * outputs.  skv_get_device_error reads and clears it.  No kernel traps,
  * asserts or spins.
+ *
+ * Why bad indices and timeouts are device error bits, not skv_status values:
+ * they depend on data the host does not see when it enqueues a call (a Top-k
+ * tensor produced on the device, a product that has not run yet), and a call
+ * must stay stream-ordered and capturable in a CUDA graph, so it cannot wait
+ * for them.  They are found on the device and reported through the sticky
+ * word; skv_status covers what the host can check when the call is made.
+ *
+ * Why the configuration gives row_bytes rather than an element count and an
+ * element size: the assembly path moves rows as bytes and never reads an
+ * element; only skv_attend interprets them, and it requires 576 bf16 (1152
+ * bytes).  row_bytes = elements x element size.
  */
 #ifndef SKV_H_
 #define SKV_H_
@@ -120,10 +138,16 @@ typedef struct {
  * device state; every request slot starts free and the hot buffer zeroed.
  * Requires R*L*T_max < 2^32 and R*L*S < 2^32.  *out receives the handle.
  * Synchronous.  Returns SKV_ERR_INVALID_ARG for a bad configuration,
- * SKV_ERR_OOM / SKV_ERR_CUDA on allocation failure (nothing is leaked). */
+ * SKV_ERR_OOM / SKV_ERR_CUDA on allocation failure (nothing is leaked).
+ * Source: [talk] agenda item 2 (the SparseKVCacheManager's host storage,
+ * device cache and index mapping); [digest] paragraph 1 (full KV on the CPU,
+ * a Top-k LRU buffer on the GPU). */
 SKV_API skv_status skv_create(const skv_config *cfg, skv_ctx **out);
 
-/* Synchronise the device and free everything.  A null ctx is a no-op. */
+/* Synchronise the device and free everything.  A null ctx is a no-op.
+ * Source: the pages are silent on tearing the manager down; this library's
+ * reading is that destroy frees what create allocated, after all enqueued
+ * work has finished. */
 SKV_API skv_status skv_destroy(skv_ctx *ctx);
 
 /* Publish a request (lifecycle step "publish"): take the lowest free request
@@ -134,7 +158,8 @@ SKV_API skv_status skv_destroy(skv_ctx *ctx);
  * is copied by the CPU.  With rows == null the caller writes the rows in place
  * through skv_pool_rows before the next skv_assemble on this request.  The
  * device reset is enqueued on `stream`.  *out_req receives the id.
- * Errors: SKV_ERR_CONTEXT_FULL (T > max_context), SKV_ERR_NO_FREE_REQUEST. */
+ * Errors: SKV_ERR_CONTEXT_FULL (T > max_context), SKV_ERR_NO_FREE_REQUEST.
+ * Source: [xm] section "与SGLang HiSparse的集成" (publish). */
 SKV_API skv_status skv_publish(skv_ctx *ctx, const void *rows, int64_t T, int32_t *out_req, skv_stream_t stream);
 
 /* Write back one new token per listed request (lifecycle step "write back"):
@@ -146,7 +171,10 @@ SKV_API skv_status skv_publish(skv_ctx *ctx, const void *rows, int64_t T, int32_
  * nothing is written.  The new token can be selected from the next
  * skv_assemble on; it is not put into the hot buffer by this call.
  * n == 0 enqueues nothing.  Host errors: n < 0 or n > max_batch, null
- * pointers with n > 0. */
+ * pointers with n > 0.
+ * Source: [xm] section "与SGLang HiSparse的集成" (write back); that the new
+ * token enters the pool only, not the hot buffer, is this library's reading
+ * (the pages name the step, not its effect on the device cache). */
 SKV_API skv_status skv_write_back(skv_ctx *ctx, const int32_t *req_ids_dev, int32_t n, const void *rows_dev,
                           skv_stream_t stream);
 
@@ -181,7 +209,12 @@ SKV_API skv_status skv_extend(skv_ctx *ctx, int32_t req, const void *rows, int64
  * The hot row of (request r, layer l, slot s) is at
  * skv_hot_buffer() + ((r*L + l)*S + s) * row_bytes.
  * Inputs and outputs are device memory, B <= max_batch.  B == 0 enqueues
- * nothing and does not advance the clock.  Captures into a CUDA graph. */
+ * nothing and does not advance the clock.  Captures into a CUDA graph.
+ * Source: [xm] section "与SGLang HiSparse的集成" (acquire; CUDA Graph
+ * support); [talk] abstract and agenda items 1-2 (token-level, Top-k-driven
+ * assembly; UniDex index copy); [digest] paragraphs 1 and 3 (Top-k LRU
+ * buffer; Sparse Diff Kernel).  The tie-break and the order in which misses
+ * take victims are this library's reading (the pages give neither). */
 SKV_API skv_status skv_assemble(skv_ctx *ctx, const int32_t *req_ids_dev, int32_t B, const int32_t *topk_dev,
                         int32_t *slots_dev, int32_t *hits_dev, int32_t *misses_dev, skv_stream_t stream);
 
@@ -253,9 +286,8 @@ SKV_API skv_status skv_assemble_host(skv_ctx *ctx, const int32_t *req_ids, int32
  * arguments, semantics and results as skv_assemble, except:
  *   - B * L * k must be <= 2^20, else SKV_ERR_INVALID_ARG (with the reason in
  *     skv_last_cuda_error) and nothing is enqueued;
- *   - the first call on a device looks up the array's device address (with
- *     that device current) and caches it: make that first call before any
- *     stream capture;
+ *   - skv_create loads the array on the context's device and looks up its
+ *     address, so no call of this entry point loads or allocates anything;
  *   - every call on a device shares the one array: calls that overlap on the
  *     GPU (other streams, other contexts) race.  Nothing in the array needs
  *     to start at zero; the step resets its own counter.
@@ -267,7 +299,8 @@ SKV_API skv_status skv_assemble_noalloc(skv_ctx *ctx, const int32_t *req_ids_dev
 /* Release a request (lifecycle step "release"): its slot becomes free, its
  * maps are reset and its hot rows zeroed (enqueued on `stream`).  A later
  * skv_publish may hand the same id out again.  SKV_ERR_BAD_REQUEST if req is
- * not an active request. */
+ * not an active request.
+ * Source: [xm] section "与SGLang HiSparse的集成" (release). */
 SKV_API skv_status skv_release(skv_ctx *ctx, int32_t req, skv_stream_t stream);
 
 /* Sparse MLA decode attention over assembled slots (the "compute" of
@@ -299,11 +332,18 @@ SKV_API skv_status skv_attend(skv_ctx *ctx, const int32_t *req_ids_dev, int32_t 
                               skv_stream_t stream);
 
 /* Read the sticky device error word into *bits (SKV_DEVERR_* mask, 0 = none)
- * and clear it.  Synchronises `stream`. */
+ * and clear it.  Synchronises `stream`.
+ * Source: the pages are silent on invalid input; this library's reading is
+ * that a call with a bad request id or a bad or repeated Top-k entry is
+ * rejected whole, and that a graph-executable step ([talk] agenda item 2,
+ * UniDex; [xm] CUDA Graph support) reports it through device memory. */
 SKV_API skv_status skv_get_device_error(skv_ctx *ctx, int32_t *bits, skv_stream_t stream);
 
 /* Device address of the hot buffer and the bytes between consecutive
- * (request, layer) units (S * row_bytes).  Either pointer may be null. */
+ * (request, layer) units (S * row_bytes).  Either pointer may be null.
+ * Source: [talk] agenda item 2 (the device cache and the index mapping that
+ * the attention kernel reads through: slot s of (r, l) is the row at
+ * base + ((r*L + l)*S + s) * row_bytes). */
 SKV_API skv_status skv_hot_buffer(skv_ctx *ctx, void **base, int64_t *unit_stride_bytes);
 
 /* Host address of the pool; row (r, l, t) is at
@@ -315,7 +355,9 @@ SKV_API skv_status skv_pool_rows(skv_ctx *ctx, void **host_base);
 /* Debug / parity: copy one request's state to host memory after synchronising
  * `stream`.  Any output pointer may be null.  slot2tok, ts, lru are [L][S]
  * (lru as int32 slot ids, least recently used first), tok2slot is
- * [L][T_max], *len the request's token count, *active 1 or 0. */
+ * [L][T_max], *len the request's token count, *active 1 or 0.
+ * Source: [talk] agenda item 2 (the index mapping it exports); the pages
+ * describe no export: it exists so the state can be checked. */
 SKV_API skv_status skv_export_state(skv_ctx *ctx, int32_t req, int32_t *slot2tok, uint32_t *ts, int32_t *tok2slot,
                             int32_t *lru, int64_t *len, int32_t *active, skv_stream_t stream);
 
@@ -364,6 +406,19 @@ SKV_API skv_status skv_set_attend_sms(skv_ctx *ctx, int32_t sms);
  * any decode step. */
 SKV_API skv_status skv_selftest_mma(const void *a_dev, const void *b_dev, float *d_dev, int32_t n, int32_t k,
                                     int32_t mode, skv_stream_t stream);
+
+/* Diagnostic of skv_attend's bounded waits (not part of any decode step):
+ * launches the attention kernel over the call's units (all layers; arguments
+ * as skv_attend, out_dev [units][128][512] bf16) exactly as skv_attend would,
+ * except that the kernel never issues a key load.  Its first wait for keys
+ * therefore runs out (within about two seconds) with no copy and no
+ * tensor-core product in flight; the kernel sets SKV_DEVERR_TIMEOUT in the
+ * sticky error word and winds down, leaving out_dev unspecified.  Lets a test
+ * show that a wait that runs out ends in an error status the host can read
+ * (skv_get_device_error) and that the context stays usable, without faulting
+ * or hanging a GPU.  Host errors as skv_attend. */
+SKV_API skv_status skv_selftest_attend_timeout(skv_ctx *ctx, const int32_t *req_ids_dev, int32_t B, const void *q_dev,
+                                               const int32_t *slots_dev, void *out_dev, skv_stream_t stream);
 
 /* The message of the last failing CUDA call on this thread ("" if none). */
 SKV_API const char *skv_last_cuda_error(void);

@@ -298,7 +298,7 @@ __device__ __forceinline__ void give_up(AttnCtl& c, uint32_t* err)
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
     attend_kernel(const __grid_constant__ CUtensorMap hot_map, Dev d, const int32_t* __restrict__ req_ids,
                   const uint16_t* __restrict__ q, const int32_t* __restrict__ slots, uint16_t* __restrict__ out,
-                  float* __restrict__ lse, float scale_log2, AttnLayout lay, int units)
+                  float* __restrict__ lse, float scale_log2, AttnLayout lay, int units, int withhold_keys)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
     AttnCtl& c = *reinterpret_cast<AttnCtl*>(smem + lay.off_ctl);
@@ -372,7 +372,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
             int last[kMaxStages] = {-1, -1, -1, -1};  // last block issued into each stage
             bool ok = true;
             int g0 = 0;  // first block of the unit
-            for (int u = cl; ok && u < units; u += ncl) {
+            // withhold_keys (the timeout self-test only): no copy is ever issued, so the first wait for
+            // keys runs out with nothing in flight
+            for (int u = cl; ok && !withhold_keys && u < units; u += ncl) {
                 int b, l;
                 const int32_t r = req_of(u, b, l);
                 if (r < 0) continue;
@@ -819,7 +821,7 @@ cudaError_t prepare_attend(int* device_sms)
 
 cudaError_t launch_attend(const void* hot_map, const Dev& d, const int32_t* req_ids, int B, const void* q,
                           const int32_t* slots, void* out, float* lse, float sm_scale, int max_sms, int device_sms,
-                          cudaStream_t st)
+                          cudaStream_t st, bool withhold_keys)
 {
     const AttnLayout lay = attend_layout();
     if (d.k > (int)kMaxTopk || lay.bytes > kSmemLimit || device_sms < 2) return cudaErrorInvalidValue;
@@ -829,15 +831,16 @@ cudaError_t launch_attend(const void* hot_map, const Dev& d, const int32_t* req_
     const int clusters = std::max(1, std::min(units, use_sms / 2));
     attend_kernel<<<clusters * 2, kAttnThreads, lay.bytes, st>>>(
         *static_cast<const CUtensorMap*>(hot_map), d, req_ids, static_cast<const uint16_t*>(q), slots,
-        static_cast<uint16_t*>(out), lse, sm_scale * 1.4426950408889634f, lay, units);
+        static_cast<uint16_t*>(out), lse, sm_scale * 1.4426950408889634f, lay, units, withhold_keys ? 1 : 0);
     return cudaGetLastError();
 }
 
 }  // namespace skv
 
-extern "C" skv_status skv_attend(skv_ctx* ctx, const int32_t* req_ids_dev, int32_t B, int32_t layer, const void* q_dev,
-                                 const int32_t* slots_dev, void* out_dev, float* lse_dev, float sm_scale,
-                                 skv_stream_t stream)
+namespace {
+skv_status attend_impl(skv_ctx* ctx, const int32_t* req_ids_dev, int32_t B, int32_t layer, const void* q_dev,
+                       const int32_t* slots_dev, void* out_dev, float* lse_dev, float sm_scale, skv_stream_t stream,
+                       bool withhold_keys, const char* what)
 {
     if (!ctx || B < 0 || B > ctx->cfg.max_batch || layer < -1 || layer >= ctx->cfg.num_layers ||
         !(sm_scale > 0.0f) || !std::isfinite(sm_scale))
@@ -858,13 +861,30 @@ extern "C" skv_status skv_attend(skv_ctx* ctx, const int32_t* req_ids_dev, int32
     d.layer_sel = layer;
     if (e == cudaSuccess)
         e = skv::launch_attend(&ctx->hot_map, d, req_ids_dev, B, q_dev, slots_dev, out_dev, lse_dev, sm_scale,
-                               ctx->attend_sms, ctx->device_sms, stream);
+                               ctx->attend_sms, ctx->device_sms, stream, withhold_keys);
     if (prev >= 0 && prev != ctx->cfg.device) cudaSetDevice(prev);
     if (e != cudaSuccess) {
-        skv::set_last_error_message((std::string("skv_attend: ") + cudaGetErrorString(e)).c_str());
+        skv::set_last_error_message((std::string(what) + ": " + cudaGetErrorString(e)).c_str());
         return SKV_ERR_CUDA;
     }
     return SKV_OK;
+}
+}  // namespace
+
+extern "C" skv_status skv_attend(skv_ctx* ctx, const int32_t* req_ids_dev, int32_t B, int32_t layer, const void* q_dev,
+                                 const int32_t* slots_dev, void* out_dev, float* lse_dev, float sm_scale,
+                                 skv_stream_t stream)
+{
+    return attend_impl(ctx, req_ids_dev, B, layer, q_dev, slots_dev, out_dev, lse_dev, sm_scale, stream, false,
+                       "skv_attend");
+}
+
+extern "C" skv_status skv_selftest_attend_timeout(skv_ctx* ctx, const int32_t* req_ids_dev, int32_t B,
+                                                  const void* q_dev, const int32_t* slots_dev, void* out_dev,
+                                                  skv_stream_t stream)
+{
+    return attend_impl(ctx, req_ids_dev, B, -1, q_dev, slots_dev, out_dev, nullptr, 1.0f, stream, true,
+                       "skv_selftest_attend_timeout");
 }
 
 extern "C" skv_status skv_set_attend_sms(skv_ctx* ctx, int32_t sms)

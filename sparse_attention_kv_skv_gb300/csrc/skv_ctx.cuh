@@ -31,4 +31,7 @@ struct skv_ctx {
 namespace skv {
 // Sets the message returned by skv_last_cuda_error on this thread.
 void set_last_error_message(const char* msg);
+// Loads skv_assemble_noalloc's static work list on `device` (current) and
+// caches its address, so that no later call loads or allocates anything.
+cudaError_t noalloc_prepare(int device);
 }  // namespace skv

@@ -83,9 +83,11 @@ size_t attend_smem_bytes(int k);
 cudaError_t encode_hot_map(const Dev& d, struct CUtensorMap_st* map);
 // hot_map: a CUtensorMap over the hot buffer as [R*L*S rows][576] bf16 (box one row x 64, 128B swizzle).
 // max_sms: SMs the kernel may occupy (0: all of device_sms, the device's count).
+// withhold_keys: the timeout self-test (no key copy is issued, so the kernel's
+// bounded waits run out with nothing in flight).
 cudaError_t launch_attend(const void* hot_map, const Dev& d, const int32_t* req_ids, int B, const void* q,
                           const int32_t* slots, void* out, float* lse, float sm_scale, int max_sms, int device_sms,
-                          cudaStream_t st);
+                          cudaStream_t st, bool withhold_keys = false);
 // Once per context, on its device: the kernel's shared-memory attribute; *device_sms = the SM count.
 cudaError_t prepare_attend(int* device_sms);
 

@@ -6,8 +6,11 @@
 // their own KV pools and graph memory pools at start-up and then forbid or
 // cannot satisfy further cudaMalloc calls; code that runs inside another
 // component's stream capture may not allocate either.  Such a caller gets
-// the work list from memory that exists as soon as the library is loaded on
-// a device.  The pages describe no such entry point; it is a deployment aid.
+// the work list from a static array that skv_create has already brought into
+// existence on the context's device: CUDA loads a translation unit's device
+// code and data lazily, and this file has no kernel that would load it, so
+// skv_create looks the array up (noalloc_prepare), which loads it there and
+// then.  The pages describe no such entry point; it is a deployment aid.
 //
 // The array is shared by every call on the device, from every context, and
 // keeps the last call's contents.  It needs no clearing: the step's own
@@ -50,6 +53,19 @@ cudaError_t jobs_address(int device, uint2** out)
     *out = g_jobs_ptr[device];
     return cudaSuccess;
 }
+
+}  // namespace
+
+// Called by skv_create with the context's device current: loads the array on
+// that device (its 8 MiB are allocated by the driver now, at create, not at a
+// later skv_assemble_noalloc) and caches its address.
+cudaError_t skv::noalloc_prepare(int device)
+{
+    uint2* p = nullptr;
+    return jobs_address(device, &p);
+}
+
+namespace {
 
 skv_status fail(const std::string& msg, skv_status s)
 {

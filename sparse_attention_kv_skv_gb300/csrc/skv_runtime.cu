@@ -9,6 +9,7 @@
 // HiSparse integration).
 
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -76,7 +77,6 @@ void free_ctx(skv_ctx* c)
     cudaFree(c->d.active);
     cudaFree(c->d.ctl);
     cudaFree(c->d.stats);
-    cudaFree(c->d.jobs);
     cudaFree(c->d.wb_pos);
     cudaFree(c->st_req);
     cudaFree(c->st_topk);
@@ -140,6 +140,22 @@ cudaError_t record_event(cudaEvent_t ev, cudaStream_t stream)
     if (cs == cudaStreamCaptureStatusActive) return cudaEventRecordWithFlags(ev, stream, cudaEventRecordExternal);
     return cudaEventRecord(ev, stream);
 }
+
+// Test hook for the allocation-failure path of skv_create: when the
+// environment variable SKV_TEST_FAIL_ALLOC=n (n >= 1) is set, the n-th
+// allocation of a create call fails with cudaErrorMemoryAllocation without
+// being attempted.  Read at every create; unset (or 0) it does nothing.  Only
+// tests set it: a real out-of-memory on a shared GPU is not something to
+// provoke.
+struct AllocFault {
+    long fail_at = 0, seen = 0;
+    AllocFault()
+    {
+        const char* v = std::getenv("SKV_TEST_FAIL_ALLOC");
+        if (v) fail_at = std::strtol(v, nullptr, 10);
+    }
+    bool next() { return fail_at > 0 && ++seen == fail_at; }
+};
 
 }  // namespace
 
@@ -211,28 +227,31 @@ skv_status skv_create(const skv_config* cfg, skv_ctx** out)
         cudaError_t e_ = (call);                     \
         if (e_ != cudaSuccess) return fail(e_, #call); \
     } while (0)
+    // an allocation, unless the test hook makes it fail
+    AllocFault fault;
+#define SKV_ALLOC(call) SKV_TRY(fault.next() ? cudaErrorMemoryAllocation : (call))
 
     const size_t pool_bytes = (size_t)units * c.max_context * c.row_bytes;
-    SKV_TRY(alloc_pool(x, pool_bytes));
+    SKV_ALLOC(alloc_pool(x, pool_bytes));
     SKV_TRY(cudaHostGetDevicePointer((void**)&d.pool, x->pool_host, 0));
-    SKV_TRY(cudaHostAlloc((void**)&x->host_word, 64, cudaHostAllocDefault));
-    SKV_TRY(cudaMalloc(&d.tok2slot, (size_t)units * c.max_context * 4));
-    SKV_TRY(cudaMalloc(&d.slot2tok, (size_t)units * c.hot_slots * 4));
-    SKV_TRY(cudaMalloc(&d.ts, (size_t)units * c.hot_slots * 4));
-    SKV_TRY(cudaMalloc(&d.lru, (size_t)units * c.hot_slots * 2));
-    SKV_TRY(cudaMalloc(&d.hot, (size_t)units * c.hot_slots * c.row_bytes));
-    SKV_TRY(cudaMalloc(&d.len, (size_t)c.max_requests * 8));
-    SKV_TRY(cudaMalloc(&d.active, (size_t)c.max_requests * 4));
-    SKV_TRY(cudaMalloc(&d.ctl, skv::CTL_WORDS * 4));
-    SKV_TRY(cudaMalloc(&d.stats, skv::STAT_WORDS * 8));
+    SKV_ALLOC(cudaHostAlloc((void**)&x->host_word, 64, cudaHostAllocDefault));
+    SKV_ALLOC(cudaMalloc(&d.tok2slot, (size_t)units * c.max_context * 4));
+    SKV_ALLOC(cudaMalloc(&d.slot2tok, (size_t)units * c.hot_slots * 4));
+    SKV_ALLOC(cudaMalloc(&d.ts, (size_t)units * c.hot_slots * 4));
+    SKV_ALLOC(cudaMalloc(&d.lru, (size_t)units * c.hot_slots * 2));
+    SKV_ALLOC(cudaMalloc(&d.hot, (size_t)units * c.hot_slots * c.row_bytes));
+    SKV_ALLOC(cudaMalloc(&d.len, (size_t)c.max_requests * 8));
+    SKV_ALLOC(cudaMalloc(&d.active, (size_t)c.max_requests * 4));
+    SKV_ALLOC(cudaMalloc(&d.ctl, skv::CTL_WORDS * 4));
+    SKV_ALLOC(cudaMalloc(&d.stats, skv::STAT_WORDS * 8));
     const size_t step_entries = (size_t)c.max_batch * c.num_layers * c.topk;
-    SKV_TRY(cudaMalloc(&d.jobs, step_entries * sizeof(uint2)));
-    SKV_TRY(cudaMalloc(&d.wb_pos, (size_t)c.max_batch * 8));
-    SKV_TRY(cudaMalloc(&x->st_req, (size_t)c.max_batch * 4));
-    SKV_TRY(cudaMalloc(&x->st_topk, step_entries * 4));
-    SKV_TRY(cudaMalloc(&x->st_slots, step_entries * 4));
-    SKV_TRY(cudaMalloc(&x->st_hits, (size_t)c.max_batch * c.num_layers * 4));
-    SKV_TRY(cudaMalloc(&x->st_misses, (size_t)c.max_batch * c.num_layers * 4));
+    d.jobs = nullptr;  // only skv_assemble_noalloc queues gather jobs, into its static array
+    SKV_ALLOC(cudaMalloc(&d.wb_pos, (size_t)c.max_batch * 8));
+    SKV_ALLOC(cudaMalloc(&x->st_req, (size_t)c.max_batch * 4));
+    SKV_ALLOC(cudaMalloc(&x->st_topk, step_entries * 4));
+    SKV_ALLOC(cudaMalloc(&x->st_slots, step_entries * 4));
+    SKV_ALLOC(cudaMalloc(&x->st_hits, (size_t)c.max_batch * c.num_layers * 4));
+    SKV_ALLOC(cudaMalloc(&x->st_misses, (size_t)c.max_batch * c.num_layers * 4));
 
     SKV_TRY(cudaMemset(d.tok2slot, 0xFF, (size_t)units * c.max_context * 4));
     SKV_TRY(cudaMemset(d.slot2tok, 0xFF, (size_t)units * c.hot_slots * 4));
@@ -246,7 +265,9 @@ skv_status skv_create(const skv_config* cfg, skv_ctx** out)
     SKV_TRY(skv::prepare_step_kernels(c.topk, c.hot_slots, &x->gather_grid));
     x->plan_resident = skv::plan_resident_ctas(c.topk, c.hot_slots);
     SKV_TRY(skv::prepare_attend(&x->device_sms));
+    SKV_TRY(skv::noalloc_prepare(c.device));
     SKV_TRY(cudaDeviceSynchronize());
+#undef SKV_ALLOC
 #undef SKV_TRY
     *out = x;
     return SKV_OK;

@@ -618,6 +618,10 @@ cudaError_t prepare_step_kernels(int k, int S, int* gather_grid)
     if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_kernel<72, kGatherUnroll>,
                                                            kGatherThreads, 0)) != cudaSuccess)
         return e;
+    // every kernel of the step is loaded here, at context creation (CUDA loads
+    // functions lazily), so that no assemble call loads code later
+    cudaFuncAttributes fa;
+    if ((e = cudaFuncGetAttributes(&fa, gather_kernel<0, kGatherUnroll>)) != cudaSuccess) return e;
     *gather_grid = sms * (per_sm > 0 ? per_sm : 1);
     return cudaSuccess;
 }

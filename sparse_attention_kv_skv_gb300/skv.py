@@ -77,6 +77,7 @@ def _load():
         "skv_set_attend_sms": [vp, i32],
         "skv_selftest_mma": [vp, vp, vp, i32, i32, i32, vp],
         "skv_attend": [vp, vp, i32, i32, vp, vp, vp, vp, ctypes.c_float, vp],
+        "skv_selftest_attend_timeout": [vp, vp, i32, vp, vp, vp, vp],
     }
     for name, args in sigs.items():
         f = getattr(lib, name)
@@ -115,6 +116,7 @@ skv_set_gather_events = lib.skv_set_gather_events
 skv_set_attend_sms = lib.skv_set_attend_sms
 skv_selftest_mma = lib.skv_selftest_mma
 skv_attend = lib.skv_attend
+skv_selftest_attend_timeout = lib.skv_selftest_attend_timeout
 skv_last_cuda_error = lib.skv_last_cuda_error
 skv_status_string = lib.skv_status_string
 
@@ -261,6 +263,13 @@ class Context:
         scale = (1.0 / 576 ** 0.5) if sm_scale is None else sm_scale
         check(skv_attend(self.h, _ptr(req_ids), B, layer, _ptr(q), _ptr(slots), _ptr(out), _ptr(lse), scale,
                          _stream_handle(stream)), "skv_attend")
+
+    def selftest_attend_timeout(self, req_ids, q, slots, out, B: int | None = None, stream=None) -> None:
+        """The attention kernel with its key loads withheld: its waits run out
+        and it reports SKV_DEVERR_TIMEOUT (see skv_selftest_attend_timeout)."""
+        B = req_ids.numel() if B is None else B
+        check(skv_selftest_attend_timeout(self.h, _ptr(req_ids), B, _ptr(q), _ptr(slots), _ptr(out),
+                                          _stream_handle(stream)), "skv_selftest_attend_timeout")
 
     # inspection ------------------------------------------------------------
     def get_device_error(self, stream=None) -> int:

@@ -23,7 +23,9 @@ RB = wl.ROW_BYTES
 
 
 class Pair:
-    def __init__(self, w: wl.Workload, req_perm=None, oracle_threads: int = 0, gen_threads: int | None = None):
+    def __init__(self, w: wl.Workload, req_perm=None, oracle_threads: int = 0, gen_threads: int | None = None,
+                 entry: str = "assemble"):
+        """entry: the Context method each step calls ("assemble" or "assemble_noalloc")."""
         self.w = w
         self.R = w.R
         self.T_max = w.max_context
@@ -33,6 +35,7 @@ class Pair:
         self.ctx = Context(Config(max_requests=self.R, num_layers=w.L, max_context=self.T_max, topk=w.k,
                                   hot_slots=w.S, max_batch=w.B, row_bytes=RB))
         self.pool = self.ctx.pool_rows()
+        self.assemble_fn = getattr(self.ctx, entry)
         self.orc = orc.Oracle(self.R, w.L, self.T_max, RB, w.k, w.S, self.pool)
         self.gen = wl.TopkStream(w, nthreads=gen_threads)
         self.generation = {}
@@ -89,14 +92,14 @@ class Pair:
 
     # ------------------------------------------------------------------ steps
     def capture(self) -> None:
-        """From now on each step replays one captured CUDA graph of
-        skv_assemble over the static input buffer (as the benchmark times it)."""
+        """From now on each step replays one captured CUDA graph of the step's
+        entry point over the static input buffer (as the benchmark times it)."""
         self.graph = torch.cuda.CUDAGraph()
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(side):
             with torch.cuda.graph(self.graph, stream=side):
-                self.ctx.assemble(self.req_dev, self.topk_dev, self.slots_dev, self.hits_dev, self.misses_dev)
+                self.assemble_fn(self.req_dev, self.topk_dev, self.slots_dev, self.hits_dev, self.misses_dev)
         torch.cuda.current_stream().wait_stream(side)
         torch.cuda.synchronize()
 
@@ -128,7 +131,7 @@ class Pair:
         if getattr(self, "graph", None) is not None:
             self.graph.replay()
         else:
-            self.ctx.assemble(self.req_dev, self.topk_dev, self.slots_dev, self.hits_dev, self.misses_dev)
+            self.assemble_fn(self.req_dev, self.topk_dev, self.slots_dev, self.hits_dev, self.misses_dev)
         e, slots, hits, misses = self.orc.assemble(self.req_ids, topk, nthreads=self.threads)
         assert e == 0
         self.total_misses += int(misses.sum())

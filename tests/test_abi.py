@@ -24,9 +24,34 @@ def declared():
 
 def test_header_declares_the_lifecycle():
     names = declared()
-    for n in ("skv_create", "skv_destroy", "skv_publish", "skv_write_back", "skv_assemble", "skv_release",
-              "skv_get_device_error", "skv_hot_buffer", "skv_export_state"):
+    for n in LIFECYCLE:
         assert n in names
+
+
+LIFECYCLE = ("skv_create", "skv_destroy", "skv_publish", "skv_write_back", "skv_assemble", "skv_release",
+             "skv_get_device_error", "skv_hot_buffer", "skv_export_state")
+
+
+def doc_comment(name: str) -> str:
+    """The comment block right above the declaration of `name`."""
+    src = open(HEADER).read()
+    m = re.search(r"/\*((?:(?!\*/).)*)\*/\s*SKV_API\s+[\w\s\*]+?\b" + name + r"\s*\(", src, flags=re.S)
+    assert m, name
+    return m.group(1)
+
+
+def test_every_lifecycle_declaration_cites_its_source():
+    """Each boundary call of the hot path states where it comes from: a page
+    section (by the header's tags) or, where the pages are silent, the
+    reading the library implements."""
+    for n in LIFECYCLE:
+        doc = doc_comment(n)
+        assert "Source:" in doc, n
+        cite = doc.split("Source:", 1)[1]
+        assert re.search(r"\[(talk|digest|xm)\]", cite) or "pages are silent" in cite, n
+    head = open(HEADER).read().split("#ifndef SKV_H_")[0]
+    for tag in ("[talk]", "[digest]", "[xm]"):
+        assert tag in head  # every tag is defined in the opening comment
 
 
 def test_every_declared_symbol_is_exported(lib_path):

@@ -1,28 +1,48 @@
 """skv_attend (tensor-core sparse MLA attention over assembled slots) against
 the fp64 attention oracle evaluated on the CPU oracle's own hot buffer (GPU).
 
-Tolerance, from the arithmetic: q and the key rows are bf16, their products
-are exact in fp32 and summed in fp32; the half of each score summed on the
-other CTA of the pair crosses over as the upper 24 bits of its fp32 (relative
-error <= 2^-16: under 5e-4 for the partials of these inputs, |partial| < 30,
-so under 2e-4 in the exponent at scale 0.35); the probabilities P enter the second product rounded to bf16 (relative error
-<= 2^-9), so |error of out| <= 2^-9 * max|V| = 2e-3 with |V| <= 1; the output
-is rounded to bf16 (another 2^-9 |out|).  The test allows 6e-3 + 6e-3 |out|
-(x3 margin) and 5e-3 on lse.
+Every tolerance is derived from the kernel's arithmetic, per unit and head,
+from the unit's own q and keys (``bounds``):
+
+  score error.  q and the key rows are bf16, so every product q_d k_d is exact
+  in fp32.  A score is summed in two halves (dims [0, 288) on one CTA of the
+  pair, [288, 576) on the other), each over 18 tensor-core steps of 16
+  products with fp32 accumulation, and the halves are added in fp32: taking
+  each step's rounding as at most 2^-22 of the magnitude it sums (generous for
+  fp32's 2^-24), the error is at most 19 * 2^-22 * A with A = sum_d |q_d k_d|.
+  One of the two halves crosses the pair as the upper 24 bits of its fp32
+  (round to nearest: relative error at most 2^-16 of that partial P).  So a
+  scaled score is off by at most
+      ds = scale * (2^-16 * max(|P0|, |P1|) + 19 * 2^-22 * A).
+  lse.  lse = log sum_j exp(s_j) moves by at most max_j ds_j when every s_j
+  moves by at most ds_j; the rest -- ex2.approx (relative error about 2^-22 a
+  term), the fp32 sums of the denominator (at most k/32 + 64 roundings of
+  2^-24 along any chain), log2f and the final scaling -- stays below
+  1e-5 + (k/32 + 64) * 2^-24.  At scale 0.35 on these inputs that is about
+  5e-4; at scale 1/24 about 6e-5, while one dropped key of a flat softmax over
+  k keys moves lse by about 1/k.
+  out.  P enters the value product rounded to bf16 (relative error at most
+  2^-8 each, so at most 2^-8 * max|V| on the normalised output), score errors
+  change the normalised weights by at most a factor exp(2 ds), and the output
+  is rounded to bf16 (at most 2^-8 |out|):
+      |out - want| <= (2^-8 + 2 ds) * max|V| + (2^-8 + 1e-5) |want|.
+Planted-key cases put one key whose score is about 8 above the others at a
+chosen position (0, 63, 64, 65, k - 1) of a unit's slot list, with a masked
+slot among the others, for k on and next to the 64-key block boundary: a key
+that is dropped, duplicated or moved to another position breaks them.
 """
 import numpy as np
 import pytest
 import torch
 
 import skv_workload as wl
+from attention_check import check_unit
 from oracle import attention as att
 
 pytestmark = pytest.mark.gpu
 
 if torch.cuda.is_available():
     from skv_pair import Pair
-
-ATOL, RTOL, LSE_ATOL = 6e-3, 6e-3, 5e-3
 
 
 def _queries(w, units):
@@ -40,13 +60,7 @@ def _check_units(p, units, slots, q, out, lse, scale):
         valid = row >= 0
         keys = np.zeros((row.size, 576))
         keys[valid] = att.bf16_rows_to_f64(hot_cache[r][l][row[valid]])
-        want, want_lse = att.attend(att.bf16_rows_to_f64(q[n].view(np.uint8)), keys, valid, scale)
-        got = att.bf16_rows_to_f64(out[n].view(np.uint8))
-        err = np.abs(got - want) - (ATOL + RTOL * np.abs(want))
-        assert err.max() <= 0, f"unit {(b, l)}: out off by {np.abs(got - want).max()}"
-        both_inf = np.isneginf(want_lse) & np.isneginf(lse[n])
-        diff = np.abs(np.where(both_inf, 0.0, lse[n] - want_lse))
-        assert np.all(diff <= LSE_ATOL), f"unit {(b, l)}: lse"
+        check_unit(q[n], keys, valid, out[n], lse[n], scale, f"unit {(b, l)}")
 
 
 @pytest.mark.parametrize("scale,sms", [(1.0 / 24.0, 0), (0.35, 0), (0.35, 4)])
@@ -195,5 +209,96 @@ def test_attention_beside_layer_assembly_on_another_stream():
             assert e == 0 and np.array_equal(slots_l[l].cpu().numpy(), o_slots)
             _check_units(p, [(b, l) for b in range(w.B)], o_slots, q[l], out_d[l].cpu().numpy().view(np.uint16),
                          lse_d[l].cpu().numpy(), 0.3)
+    finally:
+        p.close()
+
+
+PLANT_POS = (0, 63, 64, 65, -1)   # -1: the last position, k - 1
+PLANT_HEADS = (0, 37, 64, 127)    # heads of different warps and lanes
+
+
+@pytest.mark.parametrize("k", [63, 64, 65, 127, 128, 129, 2048])
+def test_planted_key_at_block_boundaries(k):
+    """Unit (b, l) holds k distinct tokens in shuffled order with one -1 slot;
+    the token at position PLANT_POS[b] is planted: heads PLANT_HEADS of q are
+    its own key row, so its score (scale 0.05 * |key|^2, about 9.6) stands
+    about 8 above every other.  The other heads are uniform queries, whose
+    nearly flat softmax makes lse move by about 1/k for a key that is dropped.
+    Run with every SM and with one cluster walking all ten units in turn."""
+    B, L, scale = 5, 2, 0.05
+    w = wl.Workload(f"plant_k{k}", B=B, L=L, ctx=max(3000, 2 * k + 100), k=k, S=k + 37, steps=1)
+    p = Pair(w)
+    try:
+        rng = np.random.default_rng(1000 + k)
+        topk = np.empty((B, L, k), np.int32)
+        plant = {}
+        for b in range(B):
+            pos = PLANT_POS[b] if 0 <= PLANT_POS[b] < k else k - 1
+            for l in range(L):
+                row = rng.permutation(w.ctx)[:k].astype(np.int32)
+                row[(pos + 1 + int(rng.integers(k - 1))) % k] = -1  # one masked slot, never the planted one
+                topk[b, l] = row
+                plant[(b, l)] = (pos, int(row[pos]))
+        p.ctx.assemble(p.req_dev, torch.from_numpy(topk).cuda(), p.slots_dev, p.hits_dev, p.misses_dev)
+        e, o_slots, _, _ = p.orc.assemble(p.req_ids, topk)
+        assert e == 0 and np.array_equal(p.slots_dev.cpu().numpy(), o_slots)
+        units = [(b, l) for b in range(B) for l in range(L)]
+        slots = o_slots.reshape(len(units), k)
+        q = _queries(w, units).copy()
+        for n, (b, l) in enumerate(units):
+            pos, tok = plant[(b, l)]
+            assert slots[n, pos] >= 0 and (slots[n] < 0).sum() == 1
+            krow = p.pool_view(p.req_ids[b])[l, tok].view(np.uint16)
+            for h in PLANT_HEADS:
+                q[n, h] = krow
+            # the construction does what it says: the planted score leads by more than 6
+            hot = p.orc.export_hot(p.req_ids[b])[l]
+            keys = att.bf16_rows_to_f64(hot[slots[n][slots[n] >= 0]])
+            kp = att.bf16_rows_to_f64(krow.view(np.uint8))
+            sc = scale * keys @ kp
+            top2 = np.sort(sc)[-2:]
+            assert top2[1] == pytest.approx(scale * kp @ kp) and top2[1] - top2[0] > 6
+        q_d = torch.from_numpy(q).cuda()
+        for sms in (0, 2):
+            out_d = torch.full((len(units), 128, 512), 0x7FC0, dtype=torch.int16, device="cuda")
+            lse_d = torch.full((len(units), 128), float("nan"), device="cuda")
+            p.ctx.set_attend_sms(sms)
+            p.ctx.attend(p.req_dev, q_d, p.slots_dev, out_d, lse_d, sm_scale=scale)
+            out = out_d.cpu().numpy().view(np.uint16)
+            lse = lse_d.cpu().numpy()
+            _check_units(p, units, slots, q, out, lse, scale)
+            assert p.ctx.get_device_error() == 0
+    finally:
+        p.close()
+
+
+def test_attention_wait_that_runs_out_reports_timeout():
+    """The kernel's bounded waits, made to run out without endangering the
+    GPU: skv_selftest_attend_timeout launches the attention kernel with its key
+    loads withheld, so its first wait for keys gives up with nothing in flight.
+    The sticky word then carries SKV_DEVERR_TIMEOUT, and the context stays
+    usable: a normal call over the same slots is right afterwards, and the
+    assembly goes on bit-exact."""
+    from sparse_attention_kv_skv_gb300 import skv
+    w = wl.Workload("attn_timeout", B=2, L=2, ctx=2000, k=128, S=256, steps=3, fresh=0.3)
+    p = Pair(w)
+    try:
+        p.step(0)
+        units = [(b, l) for b in range(w.B) for l in range(w.L)]
+        q = _queries(w, units)
+        q_d = torch.from_numpy(q).cuda()
+        out_d = torch.empty((len(units), 128, 512), dtype=torch.int16, device="cuda")
+        lse_d = torch.empty((len(units), 128), device="cuda")
+        p.ctx.selftest_attend_timeout(p.req_dev, q_d, p.slots_dev, out_d)
+        torch.cuda.synchronize()
+        assert p.ctx.get_device_error() == skv.SKV_DEVERR_TIMEOUT
+        assert p.ctx.get_device_error() == 0  # read and cleared
+        p.ctx.attend(p.req_dev, q_d, p.slots_dev, out_d, lse_d, sm_scale=0.2)
+        slots = p.slots_dev.cpu().numpy().reshape(len(units), w.k)
+        _check_units(p, units, slots, q, out_d.cpu().numpy().view(np.uint16), lse_d.cpu().numpy(), 0.2)
+        assert p.ctx.get_device_error() == 0
+        p.step(1)
+        p.step(2)
+        p.compare_state()
     finally:
         p.close()

@@ -119,3 +119,39 @@ def test_host_checked_errors():
         with pytest.raises(SkvError, match="INVALID_ARG"):
             ctx.assemble(None, e, e, e, e, B=1)
         assert ctx.get_device_error() == 0
+
+
+def _rss_bytes() -> int:
+    for line in open("/proc/self/status"):
+        if line.startswith("VmRSS:"):
+            return int(line.split()[1]) * 1024
+    return 0
+
+
+def test_allocation_failure_at_create_frees_everything(monkeypatch):
+    """Each of skv_create's 17 allocations made to fail in turn (a host-side
+    fake of the failing call, SKV_TEST_FAIL_ALLOC): the create returns
+    SKV_ERR_OOM, nothing is left behind (device memory and resident host
+    memory as before, over repeated attempts), and a later create succeeds."""
+    from sparse_attention_kv_skv_gb300 import Config, Context, skv
+    cfg = Config(max_requests=8, num_layers=2, max_context=32768, topk=256, hot_slots=4096, max_batch=8)
+    monkeypatch.delenv("SKV_TEST_FAIL_ALLOC", raising=False)
+    Context(cfg).close()  # the first create of the process loads code; measure after it
+    torch.cuda.synchronize()
+    free0, rss0 = torch.cuda.mem_get_info()[0], _rss_bytes()
+    for rounds in range(2):
+        for n in range(1, 18):
+            monkeypatch.setenv("SKV_TEST_FAIL_ALLOC", str(n))
+            with pytest.raises(SkvError) as e:
+                Context(cfg)
+            assert e.value.status == skv.SKV_ERR_OOM, (n, e.value)
+            assert b"out of memory" in skv.skv_last_cuda_error(), n
+    torch.cuda.synchronize()
+    free1, rss1 = torch.cuda.mem_get_info()[0], _rss_bytes()
+    assert free1 == free0, f"device memory leaked: {free0 - free1} bytes"
+    # the pool alone is 8 x 2 x 32768 rows x 1152 B = 604 MB; 34 leaked pools would be 20 GB
+    assert rss1 - rss0 < 256 << 20, f"host memory grew by {(rss1 - rss0) >> 20} MiB"
+    monkeypatch.setenv("SKV_TEST_FAIL_ALLOC", "18")  # past the last allocation: nothing fails
+    with Context(cfg) as ctx:
+        assert ctx.publish(100) == 0 and ctx.clock() == 0
+    monkeypatch.delenv("SKV_TEST_FAIL_ALLOC")

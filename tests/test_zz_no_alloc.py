@@ -1,9 +1,15 @@
 """skv_assemble_noalloc -- the assemble step for callers that cannot allocate
 device memory at call time (engines that reserve nearly all HBM up front,
 code running inside someone else's stream capture) -- gives the same results
-as skv_assemble.  Its gather work list is a static device array shared by all
-calls; this file is collected last so that a failure here cannot hide other
-tests' results.  (GPU)"""
+as skv_assemble and as the CPU oracle: eagerly, replayed from a captured CUDA
+graph, and with two contexts taking turns on the one static work list.  Its
+first call on a device allocates nothing (checked in a fresh process).  This
+file is collected last so that a failure here cannot hide other tests'
+results.  (GPU)"""
+import os
+import subprocess
+import sys
+
 import numpy as np
 import pytest
 import torch
@@ -14,6 +20,9 @@ pytestmark = pytest.mark.gpu
 
 if torch.cuda.is_available():
     from sparse_attention_kv_skv_gb300 import Config, Context, SkvError
+    from skv_pair import Pair
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def _context(w):
@@ -81,3 +90,89 @@ def test_noalloc_rejects_calls_beyond_its_capacity():
             ctx.publish(10)
         ctx.assemble_noalloc(req[:16], topk[:16], slots[:16], hm[:16], hm[:16], B=16)
         assert ctx.get_device_error() == 0 and ctx.clock() == 1
+
+
+def test_noalloc_matches_the_oracle():
+    """Ragged shapes, padded and shuffled rows, a permuted request subset:
+    slots and counts every step, maps, LRU order and hot rows at the end."""
+    w = wl.Workload("noalloc_orc", B=5, L=3, ctx=5000, k=300, S=701, steps=8, fresh=0.3,
+                    order=wl.ORDER_SHUFFLED, n_pad=17, max_requests=7)
+    p = Pair(w, req_perm=[6, 1, 4, 0, 3], entry="assemble_noalloc")
+    try:
+        for s in range(w.steps):
+            p.step(s)
+        p.compare_state()
+        p.compare_hot_rows(range(p.R))
+        assert p.ctx.get_device_error() == 0
+    finally:
+        p.close()
+
+
+def test_noalloc_replays_from_a_captured_graph():
+    """One eager call, then the call captured once and replayed with each
+    step's new Top-k rows in the same input buffer; the oracle decides."""
+    w = wl.Workload("noalloc_graph", B=4, L=2, ctx=6000, k=512, S=1024, steps=6, fresh=0.3)
+    p = Pair(w, entry="assemble_noalloc")
+    try:
+        p.step(0)
+        p.capture()
+        for s in range(1, w.steps):
+            p.step(s)
+        p.compare_state()
+        assert p.ctx.get_device_error() == 0
+    finally:
+        p.close()
+
+
+def test_two_contexts_take_turns_on_the_static_work_list():
+    """Two contexts of different shapes call the entry point one after the
+    other on one stream; each matches its own oracle."""
+    wa = wl.Workload("noalloc_a", B=3, L=2, ctx=4000, k=256, S=512, steps=5, fresh=0.4)
+    wb = wl.Workload("noalloc_b", B=2, L=3, ctx=3000, k=200, S=333, steps=5, fresh=0.5, order=wl.ORDER_SHUFFLED)
+    a = Pair(wa, entry="assemble_noalloc")
+    b = Pair(wb, entry="assemble_noalloc")
+    try:
+        for s in range(5):
+            a.step(s)
+            b.step(s)
+        a.compare_state()
+        b.compare_state()
+        assert a.ctx.get_device_error() == 0 and b.ctx.get_device_error() == 0
+    finally:
+        a.close()
+        b.close()
+
+
+FIRST_CALL = r"""
+import sys
+sys.path.insert(0, sys.argv[1])
+import torch
+from sparse_attention_kv_skv_gb300 import Config, Context
+ctx = Context(Config(max_requests=4, num_layers=2, max_context=4096, topk=256, hot_slots=512, max_batch=4))
+for r in range(4):
+    ctx.publish(1000)
+req = torch.arange(4, dtype=torch.int32, device="cuda")
+topk = torch.arange(256, dtype=torch.int32, device="cuda").repeat(4, 2, 1).contiguous()
+slots = torch.empty_like(topk)
+hits = torch.empty((4, 2), dtype=torch.int32, device="cuda")
+misses = torch.empty_like(hits)
+torch.cuda.synchronize()
+free0 = torch.cuda.mem_get_info()[0]
+ctx.assemble_noalloc(req, topk, slots, hits, misses)
+torch.cuda.synchronize()
+free1 = torch.cuda.mem_get_info()[0]
+assert ctx.get_device_error() == 0 and int(misses.sum()) == 4 * 2 * 256
+ctx.close()
+print("FREE", free0, free1)
+"""
+
+
+def test_first_call_in_a_fresh_process_allocates_nothing():
+    """skv_create brings the static array into existence on the context's
+    device, so the free device memory is the same before and after the first
+    skv_assemble_noalloc call of a process."""
+    r = subprocess.run([sys.executable, "-c", FIRST_CALL, ROOT], capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = [x for x in r.stdout.splitlines() if x.startswith("FREE")][-1]
+    free0, free1 = map(int, line.split()[1:])
+    assert free0 == free1, f"free device memory changed by {free0 - free1} bytes at the first call"
