@@ -373,11 +373,13 @@ SKV_API skv_status skv_get_clock(skv_ctx *ctx, uint32_t *clock, skv_stream_t str
  * assemble calls, hit entries and missed (gathered) rows. */
 SKV_API skv_status skv_get_stats(skv_ctx *ctx, uint64_t *calls, uint64_t *hits, uint64_t *misses, skv_stream_t stream);
 
-/* Optional timing hooks: when set (non-null), skv_assemble records `before`
- * just before the kernel that moves the missing rows (the fused plan + gather
- * kernel; only validation runs before it) and `after` just after it on the call's
- * stream (external event records, so they also work inside a captured
- * graph).  Pass two nulls to clear; passing exactly one null is
+/* Optional timing hooks: when set (non-null), skv_assemble and
+ * skv_assemble_layer record `before` just before the call's first kernel
+ * (validation) and `after` just after the kernel that moves the missing rows
+ * (the fused plan + gather kernel, which starts while validation runs), on
+ * the call's stream (external event records, so they also work inside a
+ * captured graph).  No event goes between the two kernels: it would keep them
+ * from overlapping.  Pass two nulls to clear; passing exactly one null is
  * SKV_ERR_INVALID_ARG.  The events belong to the caller. */
 SKV_API skv_status skv_set_gather_events(skv_ctx *ctx, skv_event_t before, skv_event_t after);
 

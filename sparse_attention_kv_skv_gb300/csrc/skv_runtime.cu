@@ -345,15 +345,18 @@ skv_status skv_write_back(skv_ctx* ctx, const int32_t* req_ids_dev, int32_t n, c
 namespace {
 // The launch sequence of one assemble call over the units described by `d`
 // (all layers, or the one in d.layer_sel).  `timed`: record the caller's
-// gather events around the fused kernel (assemble calls only, not prefetches).
+// events around the call's two kernels (assemble calls only, not prefetches).
+// The first event goes before validation, not between the two kernels: a
+// record there would keep the fused kernel from starting while validation
+// runs (a programmatic dependent launch must follow its primary directly).
 skv_status assemble_impl(skv_ctx* ctx, const Dev& d, const int32_t* req_ids_dev, int32_t B, const int32_t* topk_dev,
                          int32_t* slots_dev, int32_t* hits_dev, int32_t* misses_dev, cudaStream_t stream,
                          bool timed = true)
 {
-    SKV_CUDA(skv::launch_validate(d, req_ids_dev, B, topk_dev, stream));
     if (timed && ctx->ev_before) SKV_CUDA(record_event(ctx->ev_before, stream));
+    SKV_CUDA(skv::launch_validate(d, req_ids_dev, B, topk_dev, stream));
     SKV_CUDA(skv::launch_plan_gather(d, req_ids_dev, B, topk_dev, slots_dev, hits_dev, misses_dev, ctx->plan_resident,
-                                     stream));
+                                     ctx->device_sms, stream));
     if (timed && ctx->ev_after) SKV_CUDA(record_event(ctx->ev_after, stream));
     return SKV_OK;
 }

@@ -22,12 +22,47 @@ constexpr uint32_t kEmpty = 0xFFFFFFFFu;
 constexpr int kMaxIpt = kMaxTopk / kPlanThreads;  // Top-k entries per plan thread
 
 // ---------------------------------------------------------------------------
-// block-wide exclusive prefix sum (blockDim.x a multiple of 32, <= 1024);
-// `sh` is >= 32 words of shared memory; all threads must call it.
+// The threads that plan, and how they synchronise: the whole CTA
+// (__syncthreads), or -- when the CTA has a prefetch warp that must not be held
+// up -- the first n threads on named barrier 1.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* total, uint32_t* sh)
+template <bool kNamed>
+struct PlanSync {
+    int n;  // planning threads: blockDim.x, or the first n (a multiple of 32)
+    __device__ __forceinline__ void sync() const
+    {
+        if (kNamed)
+            asm volatile("bar.sync 1, %0;" ::"r"(n) : "memory");
+        else
+            __syncthreads();
+    }
+    __device__ __forceinline__ bool any(bool p) const
+    {
+        if (!kNamed) return __syncthreads_or(p) != 0;
+        uint32_t r;
+        asm volatile("{\n .reg .pred q, o;\n setp.ne.u32 q, %1, 0;\n bar.red.or.pred o, 1, %2, q;\n selp.u32 %0, 1, 0, o;\n}\n"
+                     : "=r"(r) : "r"((uint32_t)p), "r"(n) : "memory");
+        return r != 0;
+    }
+    __device__ __forceinline__ bool all(bool p) const
+    {
+        if (!kNamed) return __syncthreads_and(p) != 0;
+        uint32_t r;
+        asm volatile("{\n .reg .pred q, o;\n setp.ne.u32 q, %1, 0;\n bar.red.and.pred o, 1, %2, q;\n selp.u32 %0, 1, 0, o;\n}\n"
+                     : "=r"(r) : "r"((uint32_t)p), "r"(n) : "memory");
+        return r != 0;
+    }
+};
+using CtaSync = PlanSync<false>;
+
+// ---------------------------------------------------------------------------
+// block-wide exclusive prefix sum over the syncing threads (a multiple of 32,
+// <= 1024); `sh` is >= 32 words of shared memory; all of them must call it.
+// ---------------------------------------------------------------------------
+template <class Sync>
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* total, uint32_t* sh, const Sync& sy)
 {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = sy.n >> 5;
     uint32_t x = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -35,7 +70,7 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* total,
         if (lane >= o) x += y;
     }
     if (lane == 31) sh[warp] = x;
-    __syncthreads();
+    sy.sync();
     if (warp == 0) {
         uint32_t w = lane < nw ? sh[lane] : 0u;
 #pragma unroll
@@ -45,18 +80,19 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* total,
         }
         if (lane < nw) sh[lane] = w;
     }
-    __syncthreads();
+    sy.sync();
     const uint32_t before = warp > 0 ? sh[warp - 1] : 0u;
     *total = sh[nw - 1];
-    __syncthreads();
+    sy.sync();
     return before + x - v;
 }
 
 // block-wide exclusive max over int32 values (identity -1); same calling
 // rules as block_excl_scan.
-__device__ __forceinline__ int32_t block_excl_max(int32_t v, int32_t* sh)
+template <class Sync>
+__device__ __forceinline__ int32_t block_excl_max(int32_t v, int32_t* sh, const Sync& sy)
 {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = sy.n >> 5;
     int32_t x = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -66,7 +102,7 @@ __device__ __forceinline__ int32_t block_excl_max(int32_t v, int32_t* sh)
     int32_t before_in_warp = __shfl_up_sync(0xFFFFFFFFu, x, 1);
     if (lane == 0) before_in_warp = -1;
     if (lane == 31) sh[warp] = x;
-    __syncthreads();
+    sy.sync();
     if (warp == 0) {
         int32_t w = lane < nw ? sh[lane] : -1;
 #pragma unroll
@@ -76,9 +112,9 @@ __device__ __forceinline__ int32_t block_excl_max(int32_t v, int32_t* sh)
         }
         if (lane < nw) sh[lane] = w;
     }
-    __syncthreads();
+    sy.sync();
     const int32_t before = warp > 0 ? sh[warp - 1] : -1;
-    __syncthreads();
+    sy.sync();
     return max(before, before_in_warp);
 }
 
@@ -148,7 +184,7 @@ __global__ void __launch_bounds__(kValidateThreads) validate_kernel(Dev d, const
     }
     // the row is strictly ascending iff every segment is and each segment's
     // first entry exceeds the largest entry before it
-    const int32_t before = block_excl_max(prev, scan_sh);
+    const int32_t before = block_excl_max(prev, scan_sh, CtaSync{(int)blockDim.x});
     if (first != -1 && first <= before) asc = false;
     if (!__syncthreads_and(asc)) {
         const int H = 1 << table_log2;
@@ -261,7 +297,14 @@ __device__ __forceinline__ void finish_call(const Dev& d)
     }
 }
 
+// 16-byte loads each thread keeps in flight in the fused gather: 4 when CTAs
+// share SMs (3 per SM; many units keep the link busy together), 8 when every
+// unit has an SM to itself (few units: each CTA must cover the link latency
+// alone; a bare gather of 16 units x 410 scattered rows took 67 us with 4
+// loads in flight a thread and 45 us with 16 or with the rows prefetched into
+// L2 first, as the prefetch warp does).
 constexpr int kFusedUnroll = 4;
+constexpr int kFewUnitsUnroll = 8;
 
 // Fetch `bytes` (multiple of 16, 16-byte aligned) at a global address into L2
 // without waiting for it.
@@ -284,17 +327,28 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes)
 // the call is known to be accepted.  `prefetch_rows` caps how many of this
 // unit's missing rows are prefetched into L2 as soon as they are known (a
 // budget so that all resident CTAs' prefetches fit in L2).
-template <bool kFused, int CPR_CONST>
-__global__ void __launch_bounds__(kPlanThreads, 3) plan_kernel(Dev d, const int32_t* __restrict__ req_ids,
-                                                            const int32_t* __restrict__ topk,
-                                                            int32_t* __restrict__ slots_out,
-                                                            int32_t* __restrict__ hits_out,
-                                                            int32_t* __restrict__ misses_out, int prefetch_rows)
+//
+// kPfWarp: the CTA has a seventeenth warp that issues those
+// prefetches.  A bulk prefetch instruction waits while the link is busy (up to
+// tens of microseconds for a few hundred rows per SM), so planning threads
+// that issued them themselves stood still; the prefetch warp takes the sorted
+// miss list through named barrier 2 and the kPlanThreads planning threads
+// synchronise among themselves on named barrier 1, so planning, map updates
+// and the gather run on while the prefetches queue.  The whole CTA meets only
+// at the end (finish_call).
+template <bool kFused, int CPR_CONST, int UNR = kFusedUnroll, int MINB = 3, bool kPfWarp = false>
+__global__ void __launch_bounds__(kPfWarp ? kPlanThreads + 32 : kPlanThreads, MINB)
+    plan_kernel(Dev d, const int32_t* __restrict__ req_ids, const int32_t* __restrict__ topk,
+                int32_t* __restrict__ slots_out, int32_t* __restrict__ hits_out, int32_t* __restrict__ misses_out,
+                int prefetch_rows)
 {
+    static_assert(!kPfWarp || kFused, "the prefetch warp belongs to the fused kernel");
     extern __shared__ __align__(16) uint8_t smem_raw[];
     __shared__ uint32_t scan_sh[32];
     __shared__ uint32_t job_base_sh;
-    const int tid = threadIdx.x, NT = blockDim.x;
+    __shared__ uint32_t pf_count_sh;  // rows the prefetch warp pulls into L2
+    const int tid = threadIdx.x, NT = kPfWarp ? (int)blockDim.x - 32 : (int)blockDim.x;  // NT planning threads
+    const PlanSync<kPfWarp> sy{NT};
     const int k = d.k, S = d.S;
     const int cpr = CPR_CONST > 0 ? CPR_CONST : d.row_bytes / 16;
     const int32_t* row = topk + (size_t)blockIdx.x * k;
@@ -314,6 +368,19 @@ __global__ void __launch_bounds__(kPlanThreads, 3) plan_kernel(Dev d, const int3
     const int ipt = (k + NT - 1) / NT;
     const int i0 = tid * ipt;
     int m = 0, h = 0;
+
+    if (kPfWarp && tid >= NT) {
+        // the prefetch warp: the planners hand over the sorted miss list (named barrier 2, which they
+        // pass on every path, also a rejected one); the rows were bounds-checked against the pool
+        // allocation, so the prefetches may run before validation has finished
+        asm volatile("bar.sync 2, %0;" ::"r"(NT + 32) : "memory");
+        const int npf = (int)pf_count_sh;
+        const uint8_t* src = d.pool + (size_t)u * d.T_max * d.row_bytes;
+        for (int j = tid - NT; j < npf; j += 32)
+            prefetch_l2(src + (size_t)(sm.miss[j] >> 32) * d.row_bytes, (uint32_t)d.row_bytes);
+        finish_call(d);  // the CTA's one meeting of all its threads
+        return;
+    }
 
     if (r_ok) {
         for (int w = tid; w < SW; w += NT) {
@@ -339,7 +406,7 @@ __global__ void __launch_bounds__(kPlanThreads, 3) plan_kernel(Dev d, const int3
             const int32_t t = tok[j];
             hit_slot[j] = (t >= 0 && (int64_t)t < d.T_max) ? t2s[t] : -1;
         }
-        __syncthreads();  // bitmaps zeroed, LRU order loaded
+        sy.sync();  // bitmaps zeroed, LRU order loaded
         uint32_t missmask = 0, nmiss = 0, nhit = 0;
 #pragma unroll
         for (int j = 0; j < kMaxIpt; ++j) {
@@ -358,12 +425,12 @@ __global__ void __launch_bounds__(kPlanThreads, 3) plan_kernel(Dev d, const int3
                 ++nmiss;
                 // the budget covers every possible miss of this unit: start
                 // pulling the row over the host link right away
-                if (prefetch_rows >= k)
+                if (!kPfWarp && prefetch_rows >= k)
                     prefetch_l2(d.pool + ((size_t)u * d.T_max + t) * d.row_bytes, (uint32_t)d.row_bytes);
             }
         }
         uint32_t total;
-        const uint32_t excl = block_excl_scan(nmiss | (nhit << 16), &total, scan_sh);
+        const uint32_t excl = block_excl_scan(nmiss | (nhit << 16), &total, scan_sh, sy);
         m = (int)(total & 0xFFFFu);
         h = (int)(total >> 16);
         {
@@ -373,16 +440,16 @@ __global__ void __launch_bounds__(kPlanThreads, 3) plan_kernel(Dev d, const int3
                 if (missmask & (1u << j))
                     sm.miss[o++] = ((unsigned long long)(uint32_t)tok[j] << 32) | (uint32_t)(i0 + j);
         }
-        __syncthreads();
+        sy.sync();
 
         // B. misses in ascending token order
         int unsorted = 0;
         for (int j = tid; j + 1 < m; j += NT)
             if ((sm.miss[j] >> 32) > (sm.miss[j + 1] >> 32)) unsorted = 1;
-        if (__syncthreads_or(unsorted)) {
+        if (sy.any(unsorted)) {
             const int P = next_pow2(m);
             for (int j = m + tid; j < P; j += NT) sm.miss[j] = ~0ull;
-            __syncthreads();
+            sy.sync();
             for (int size = 2; size <= P; size <<= 1) {
                 for (int stride = size >> 1; stride > 0; stride >>= 1) {
                     for (int i = tid; i < P / 2; i += NT) {
@@ -394,14 +461,17 @@ __global__ void __launch_bounds__(kPlanThreads, 3) plan_kernel(Dev d, const int3
                             sm.miss[hi] = a;
                         }
                     }
-                    __syncthreads();
+                    sy.sync();
                 }
             }
         }
 
         // the missing rows are known: start pulling (the first) of them over
         // the host link while the LRU work below runs
-        if (prefetch_rows < k) {  // otherwise every row was prefetched in phase A
+        if (kPfWarp) {
+            if (tid == 0) pf_count_sh = (uint32_t)(m < prefetch_rows ? m : prefetch_rows);
+            asm volatile("bar.arrive 2, %0;" ::"r"(NT + 32) : "memory");
+        } else if (prefetch_rows < k) {  // otherwise every row was prefetched in phase A
             const int npf = m < prefetch_rows ? m : prefetch_rows;
             const uint8_t* src = d.pool + (size_t)u * d.T_max * d.row_bytes;
             for (int j = tid; j < npf; j += NT)
@@ -417,7 +487,7 @@ __global__ void __launch_bounds__(kPlanThreads, 3) plan_kernel(Dev d, const int3
             if (p < S && !bit_test(sm.hitbits, sm.lru_old[p])) ++cnt;
         }
         uint32_t tot2;
-        uint32_t rank = block_excl_scan(cnt, &tot2, scan_sh);
+        uint32_t rank = block_excl_scan(cnt, &tot2, scan_sh, sy);
         for (int j = 0; j < spt; ++j) {
             const int p = p0 + j;
             if (p >= S) break;
@@ -431,7 +501,7 @@ __global__ void __launch_bounds__(kPlanThreads, 3) plan_kernel(Dev d, const int3
             }
             ++rank;
         }
-        __syncthreads();
+        sy.sync();
 
         // D. the slots used by this step go to the back, by slot index
         const int untouched = S - h - m;
@@ -441,12 +511,15 @@ __global__ void __launch_bounds__(kPlanThreads, 3) plan_kernel(Dev d, const int3
             if (s < S && (bit_test(sm.hitbits, s) || bit_test(sm.vicbits, s))) ++cnt3;
         }
         uint32_t tot3;
-        uint32_t pos = block_excl_scan(cnt3, &tot3, scan_sh);
+        uint32_t pos = block_excl_scan(cnt3, &tot3, scan_sh, sy);
         for (int j = 0; j < spt; ++j) {
             const int s = p0 + j;
             if (s < S && (bit_test(sm.hitbits, s) || bit_test(sm.vicbits, s)) && untouched + (int)pos < S && untouched >= 0)
                 sm.lru_new[untouched + pos++] = (uint16_t)s;
         }
+    } else if (kPfWarp) {  // not a request: nothing to prefetch, but the prefetch warp waits for the count
+        if (tid == 0) pf_count_sh = 0u;
+        asm volatile("bar.arrive 2, %0;" ::"r"(NT + 32) : "memory");
     }
 
     // nothing global has been written yet; from here on the call must be known valid
@@ -468,7 +541,7 @@ __global__ void __launch_bounds__(kPlanThreads, 3) plan_kernel(Dev d, const int3
         if (s >= 0) tsu[s] = now1;  // hit
     }
     if (!kFused && tid == 0) job_base_sh = m ? atomicAdd(&d.ctl[CTL_JOBS], (uint32_t)m) : 0u;
-    __syncthreads();
+    sy.sync();
     for (int j = tid; j < m; j += NT) {
         const int v = sm.victim[j];
         const unsigned long long key = sm.miss[j];
@@ -482,7 +555,7 @@ __global__ void __launch_bounds__(kPlanThreads, 3) plan_kernel(Dev d, const int3
         sm.out[i] = v;
         if (!kFused) d.jobs[job_base_sh + j] = make_uint2((uint32_t)(u * d.T_max + t), (uint32_t)(u * S + v));
     }
-    __syncthreads();
+    sy.sync();
 
     for (int i = tid; i < k; i += NT) out[i] = sm.out[i];
     if ((S & 7) == 0) {
@@ -504,22 +577,22 @@ __global__ void __launch_bounds__(kPlanThreads, 3) plan_kernel(Dev d, const int3
         const int4* __restrict__ src = reinterpret_cast<const int4*>(d.pool) + (size_t)u * d.T_max * cpr;
         int4* __restrict__ dst = reinterpret_cast<int4*>(d.hot) + (size_t)u * S * cpr;
         const int chunks = m * cpr;
-        for (int base = tid; base < chunks; base += NT * kFusedUnroll) {
-            int4 v[kFusedUnroll];
-            size_t o[kFusedUnroll];
+        for (int base = tid; base < chunks; base += NT * UNR) {
+            int4 v[UNR];
+            uint32_t o[UNR];  // victim * cpr + w < S * cpr <= 2^14 * 2^12
 #pragma unroll
-            for (int j = 0; j < kFusedUnroll; ++j) {
+            for (int j = 0; j < UNR; ++j) {
                 const int c = base + j * NT;
                 if (c < chunks) {
                     const int jj = c / cpr;
                     const int w = c - jj * cpr;
                     const int32_t t = (int32_t)(sm.miss[jj] >> 32);
-                    o[j] = (size_t)sm.victim[jj] * cpr + w;
+                    o[j] = (uint32_t)sm.victim[jj] * (uint32_t)cpr + (uint32_t)w;
                     v[j] = ld_stream(src + (size_t)t * cpr + w);
                 }
             }
 #pragma unroll
-            for (int j = 0; j < kFusedUnroll; ++j)
+            for (int j = 0; j < UNR; ++j)
                 if (base + j * NT < chunks) st_stream(dst + o[j], v[j]);
         }
         finish_call(d);
@@ -609,6 +682,12 @@ cudaError_t prepare_step_kernels(int k, int S, int* gather_grid)
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(plan_kernel<true, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, plan_max);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(plan_kernel<true, 72, kFewUnitsUnroll, 1, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, plan_max);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(plan_kernel<true, 0, kFewUnitsUnroll, 1, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, plan_max);
+    if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(validate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)validate_smem_bytes(kMaxTopk));
     if (e != cudaSuccess) return e;
@@ -650,7 +729,7 @@ cudaError_t launch_plan(const Dev& d, const int32_t* req_ids, int B, const int32
 }
 
 cudaError_t launch_plan_gather(const Dev& d, const int32_t* req_ids, int B, const int32_t* topk, int32_t* slots,
-                               int32_t* hits, int32_t* misses, int resident_ctas, cudaStream_t st)
+                               int32_t* hits, int32_t* misses, int resident_ctas, int device_sms, cudaStream_t st)
 {
     // L2 prefetch of the missing rows pays only when every CTA is resident at
     // once (few units: planning is otherwise exposed); with more units than
@@ -658,19 +737,32 @@ cudaError_t launch_plan_gather(const Dev& d, const int32_t* req_ids, int B, cons
     // lines compete with the streaming gather (measured: -1.5 % to -4 %)
     const int grid = call_units(d, B);
     const int prefetch_rows = grid <= resident_ctas ? (int)((kPrefetchBudgetBytes / d.row_bytes) / grid) : 0;
+    // few units (at most one per SM): the variant with a prefetch warp and more loads in flight per thread
+    const bool few = grid <= device_sms;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kPlanThreads);
+    cfg.blockDim = dim3(few ? kPlanThreads + 32 : kPlanThreads);
     cfg.dynamicSmemBytes = plan_smem_bytes(d.k, d.S);
     cfg.stream = st;
+    // Programmatic dependent launch (planning overlaps validation) only for
+    // few units, at most one CTA per SM: measured 55 us from validation's
+    // start to the commit with it, 62 us without, for 16 units.  With more
+    // units it costs time: 3.016 ms a step with it and 2.947 ms without for
+    // 1536 units in waves, and 3.61 ms against 3.25 ms for eight calls of 192
+    // (co-resident, three CTAs to an SM).
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = few ? 1 : 0;
     if (d.row_bytes == 1152)
-        return cudaLaunchKernelEx(&cfg, plan_kernel<true, 72>, d, req_ids, topk, slots, hits, misses, prefetch_rows);
-    return cudaLaunchKernelEx(&cfg, plan_kernel<true, 0>, d, req_ids, topk, slots, hits, misses, prefetch_rows);
+        return few ? cudaLaunchKernelEx(&cfg, plan_kernel<true, 72, kFewUnitsUnroll, 1, true>, d, req_ids, topk, slots,
+                                        hits, misses, prefetch_rows)
+                   : cudaLaunchKernelEx(&cfg, plan_kernel<true, 72>, d, req_ids, topk, slots, hits, misses,
+                                        prefetch_rows);
+    return few ? cudaLaunchKernelEx(&cfg, plan_kernel<true, 0, kFewUnitsUnroll, 1, true>, d, req_ids, topk, slots, hits,
+                                    misses, prefetch_rows)
+               : cudaLaunchKernelEx(&cfg, plan_kernel<true, 0>, d, req_ids, topk, slots, hits, misses, prefetch_rows);
 }
 
 int plan_resident_ctas(int k, int S)
