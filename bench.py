@@ -249,8 +249,8 @@ def hbm_peak_gbs():
 # dram__bytes_read.sum + dram__bytes_write.sum.  Valid only while the kernel
 # source is the one that was captured; scaled to other workloads by units.
 PROFILED_TRAFFIC = {"source": "sparse_attention_kv_skv_gb300/csrc/skv_step_kernels.cu",
-                    "sha256": "8d62c9430bfe062f37f24aee3d4a0a50e36097b789fc6c89a43000a43cf221c6",
-                    "units": 512, "dram_bytes": 42.504192e6 + 197.452800e6}
+                    "sha256": "77ea5d673cac3fe5ae03ba3855c1bca7b2030c1b0f0d770112234e1089528878",
+                    "units": 512, "dram_bytes": 42.495488e6 + 195.300608e6}
 
 
 def profiled_traffic(w: wl.Workload):
