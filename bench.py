@@ -474,6 +474,7 @@ def run_ours(args):
     ctx = Context(Config(max_requests=w.B, num_layers=w.L, max_context=T_max, topk=w.k, hot_slots=w.S,
                          max_batch=w.B, row_bytes=rb, device=local))
     pool = ctx.pool_rows()
+    placement = ctx.pool_placement()  # host NUMA node asked for and seen (-1: none / not reported)
     for r in range(w.B):
         assert ctx.publish(w.ctx) == r
     torch.cuda.synchronize()
@@ -780,7 +781,8 @@ def run_ours(args):
                             + sum(2 * w.B for s in range(W, n_dev) if new_turn(s)),
             "clocks": clocks,
             "cpu_baseline": cpu,
-            "setup": {"pool_gb": w.pool_bytes() / 1e9, "pool_fill_s": fill_s},
+            "setup": {"pool_gb": w.pool_bytes() / 1e9, "pool_fill_s": fill_s,
+                      "pool_numa": dict(zip(("wanted_node", "seen_node", "seen_frac"), placement))},
         }
         print(json.dumps(out), flush=True)
     ctx.close()

@@ -373,6 +373,32 @@ SKV_API skv_status skv_get_clock(skv_ctx *ctx, uint32_t *clock, skv_stream_t str
  * assemble calls, hit entries and missed (gathered) rows. */
 SKV_API skv_status skv_get_stats(skv_ctx *ctx, uint64_t *calls, uint64_t *hits, uint64_t *misses, skv_stream_t stream);
 
+/* Where skv_create put the host pool.  On a host with several memory nodes
+ * (a tray with two Grace CPUs, each linked to its own GPUs) a pool on the far
+ * node would make every gather cross the CPU-to-CPU link as well, so
+ * skv_create allocates the pool under a "preferred node" memory policy for the
+ * host node nearest the context's GPU (skv_host_node_for_pci on "/sys"; the
+ * environment variable SKV_POOL_NODE overrides it: a node id, or -1 for no
+ * preference) and restores the caller's policy afterwards.
+ *   *wanted_node  the node asked for, -1 if none;
+ *   *seen_node    the node holding most of a sample of 64 pool pages as the
+ *                 kernel reports them (move_pages), -1 if it reports none;
+ *   *seen_frac    the share of that sample on *seen_node.
+ * Any output pointer may be null.
+ * Source: the pages are silent on host memory placement; the four decode GPUs
+ * of [xm] section "XM-Sparse测试平台与解码性能" each serve their own batch,
+ * which on a multi-socket host means one pool per GPU, each near its GPU. */
+SKV_API skv_status skv_pool_placement(skv_ctx *ctx, int32_t *wanted_node, int32_t *seen_node, float *seen_frac);
+
+/* The host NUMA node nearest a PCI device, read from a sysfs tree (host
+ * code only; needs no GPU): the node whose CPU list shares the most CPUs with
+ * the device's local_cpulist (lowest id on a tie); without a local CPU list,
+ * the device's numa_node if that node has CPUs (a node without CPUs may be
+ * GPU memory); else -1.  sysfs_root: null for "/sys" (a test passes a fake
+ * tree); pci_bus_id as cudaDeviceGetPCIBusId prints it ("0000:01:00.0" or
+ * with an 8-digit domain).  SKV_ERR_INVALID_ARG for null id or output. */
+SKV_API skv_status skv_host_node_for_pci(const char *sysfs_root, const char *pci_bus_id, int32_t *node);
+
 /* Optional timing hooks: when set (non-null), skv_assemble and
  * skv_assemble_layer record `before` just before the call's first kernel
  * (validation) and `after` just after the kernel that moves the missing rows

@@ -26,6 +26,9 @@ struct skv_ctx {
     bool hot_map_ready = false;
     int attend_sms = 0;     // SMs the attention kernel may occupy (0: all)
     int device_sms = 0;     // SMs of the context's device
+    int pool_node_wanted = -1;   // host NUMA node the pool was asked to live on (-1: none)
+    int pool_node_seen = -1;     // node holding most sampled pool pages (-1: not reported)
+    float pool_node_frac = 0.0f; // share of the sampled pages on pool_node_seen
 };
 
 namespace skv {

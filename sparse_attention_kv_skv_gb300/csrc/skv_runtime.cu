@@ -8,6 +8,12 @@
 // back and release ("XM-Sparse: Netpreme X-Mem ...", section on the SGLang
 // HiSparse integration).
 
+#include <dirent.h>
+#include <sys/syscall.h>
+#include <unistd.h>
+
+#include <algorithm>
+#include <cctype>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -88,6 +94,168 @@ void free_ctx(skv_ctx* c)
     delete c;
 }
 
+// ---------------------------------------------------------------------------
+// NUMA placement of the host pool.  On a host with several memory nodes (two
+// Grace CPUs to a tray, each linked to its own GPUs), a pool on the far node
+// makes every gather cross the CPU-to-CPU link as well.  The node nearest the
+// GPU is the one whose CPUs are the PCI device's local CPUs (sysfs, read
+// only); the pool is allocated under a preferred-node memory policy for that
+// node, and the caller's policy is restored afterwards.
+// ---------------------------------------------------------------------------
+constexpr int kMaxNodes = 1024;  // node ids this code handles (bits of the masks below)
+constexpr long kMpolDefault = 0, kMpolPreferred = 1;
+
+std::string read_text(const std::string& path)
+{
+    std::string out;
+    FILE* f = std::fopen(path.c_str(), "r");
+    if (!f) return out;
+    char buf[4096];
+    size_t n;
+    while ((n = std::fread(buf, 1, sizeof buf, f)) > 0) out.append(buf, n);
+    std::fclose(f);
+    while (!out.empty() && std::isspace((unsigned char)out.back())) out.pop_back();
+    return out;
+}
+
+// "0-3,8,10-11" -> {0,1,2,3,8,10,11}; false on a malformed list
+bool parse_cpulist(const std::string& s, std::vector<int>& cpus)
+{
+    cpus.clear();
+    size_t i = 0;
+    while (i < s.size()) {
+        char* end = nullptr;
+        const long a = std::strtol(s.c_str() + i, &end, 10);
+        if (end == s.c_str() + i || a < 0) return false;
+        i = (size_t)(end - s.c_str());
+        long b = a;
+        if (i < s.size() && s[i] == '-') {
+            ++i;
+            b = std::strtol(s.c_str() + i, &end, 10);
+            if (end == s.c_str() + i || b < a || b - a > 65536) return false;
+            i = (size_t)(end - s.c_str());
+        }
+        for (long c = a; c <= b; ++c) cpus.push_back((int)c);
+        if (i < s.size()) {
+            if (s[i] != ',') return false;
+            ++i;
+        }
+    }
+    return true;
+}
+
+// sysfs name of a PCI bus id as CUDA prints it ("0000:01:00.0", or with an
+// 8-digit domain): lower case, 4-digit domain
+std::string sysfs_bus_id(const char* id)
+{
+    std::string s(id);
+    for (auto& c : s) c = (char)std::tolower((unsigned char)c);
+    const size_t colon = s.find(':');
+    if (colon != std::string::npos && colon > 4) s = s.substr(colon - 4);
+    return s;
+}
+
+int host_node_for_pci(const std::string& sysfs, const std::string& bus_id)
+{
+    const std::string dev = sysfs + "/bus/pci/devices/" + bus_id;
+    std::vector<int> local;
+    const bool have_local = parse_cpulist(read_text(dev + "/local_cpulist"), local) && !local.empty();
+    const std::string nodes_dir = sysfs + "/devices/system/node";
+    int best = -1;
+    size_t best_overlap = 0;
+    std::vector<int> with_cpus;
+    if (DIR* dir = opendir(nodes_dir.c_str())) {
+        while (dirent* e = readdir(dir)) {
+            if (std::strncmp(e->d_name, "node", 4) != 0 || !std::isdigit((unsigned char)e->d_name[4])) continue;
+            const int node = std::atoi(e->d_name + 4);
+            std::vector<int> cpus;
+            if (!parse_cpulist(read_text(nodes_dir + "/" + e->d_name + "/cpulist"), cpus) || cpus.empty()) continue;
+            with_cpus.push_back(node);
+            if (!have_local) continue;
+            size_t overlap = 0;
+            for (int c : cpus) overlap += std::count(local.begin(), local.end(), c) > 0;
+            if (overlap > best_overlap || (overlap == best_overlap && overlap > 0 && node < best)) {
+                best_overlap = overlap;
+                best = node;
+            }
+        }
+        closedir(dir);
+    }
+    if (best >= 0) return best;
+    // no local CPU list: the device's own node, if that node has CPUs (a node
+    // without CPUs may be GPU memory itself)
+    const std::string nn = read_text(dev + "/numa_node");
+    if (!nn.empty()) {
+        const int node = std::atoi(nn.c_str());
+        if (node >= 0 && std::find(with_cpus.begin(), with_cpus.end(), node) != with_cpus.end()) return node;
+    }
+    return -1;
+}
+
+// The calling thread's memory policy set to "prefer `node`" for the lifetime
+// of the object, then put back as it was.  Does nothing for node < 0.
+struct PreferNode {
+    long old_mode = kMpolDefault;
+    unsigned long old_mask[kMaxNodes / 64] = {};
+    bool active = false;
+    explicit PreferNode(int node)
+    {
+        if (node < 0 || node >= kMaxNodes) return;
+        int mode = 0;
+        if (syscall(SYS_get_mempolicy, &mode, old_mask, (unsigned long)kMaxNodes + 1, nullptr, 0ul) != 0) return;
+        old_mode = mode;
+        unsigned long mask[kMaxNodes / 64] = {};
+        mask[node / 64] = 1ul << (node % 64);
+        active = syscall(SYS_set_mempolicy, kMpolPreferred, mask, (unsigned long)kMaxNodes + 1) == 0;
+    }
+    ~PreferNode()
+    {
+        if (active) syscall(SYS_set_mempolicy, old_mode, old_mask, (unsigned long)kMaxNodes + 1);
+    }
+};
+
+// The node holding most of a sample of pages of [base, base + bytes), and the
+// share of the sample there; -1 if the kernel reports no node for them.
+void sample_placement(const void* base, size_t bytes, int* node, float* frac)
+{
+    *node = -1;
+    *frac = 0.0f;
+    const long page = sysconf(_SC_PAGESIZE);
+    if (!base || bytes == 0 || page <= 0) return;
+    constexpr int kSamples = 64;
+    void* pages[kSamples];
+    int status[kSamples];
+    int n = 0;
+    for (int i = 0; i < kSamples; ++i) {
+        const size_t off = (size_t)((double)bytes * i / kSamples) / (size_t)page * (size_t)page;
+        if (off < bytes) pages[n++] = (void*)((const char*)base + off);
+    }
+    if (syscall(SYS_move_pages, 0, (unsigned long)n, pages, nullptr, status, 0) != 0) return;
+    std::vector<int> count;
+    for (int i = 0; i < n; ++i)
+        if (status[i] >= 0 && status[i] < kMaxNodes) {
+            if ((int)count.size() <= status[i]) count.resize(status[i] + 1, 0);
+            ++count[status[i]];
+        }
+    if (count.empty()) return;
+    const int best = (int)(std::max_element(count.begin(), count.end()) - count.begin());
+    *node = best;
+    *frac = (float)count[best] / (float)n;
+}
+
+// The node the pool of a context on `device` should live on: SKV_POOL_NODE if
+// set (-1: no preference), else the host node nearest the device.
+int pool_node_for_device(int device)
+{
+    if (const char* v = std::getenv("SKV_POOL_NODE")) return std::atoi(v);
+    char bus[64] = {};
+    if (cudaDeviceGetPCIBusId(bus, (int)sizeof bus, device) != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    return host_node_for_pci("/sys", sysfs_bus_id(bus));
+}
+
 // The host pool: pinned and mapped for the device with cudaHostAlloc.  (A
 // huge-page mapping registered with cudaHostRegister was tried: a stand-alone
 // gather over it starts faster, but once the CPU writes the published rows into
@@ -95,7 +263,24 @@ void free_ctx(skv_ctx* c)
 // below link speed for many steps on GB300, so it is not used.)
 cudaError_t alloc_pool(skv_ctx* x, size_t bytes)
 {
-    return cudaHostAlloc((void**)&x->pool_host, bytes, cudaHostAllocMapped | cudaHostAllocPortable);
+    try {  // no C++ exception may leave a C entry point: without a topology, no preference
+        x->pool_node_wanted = pool_node_for_device(x->cfg.device);
+    } catch (...) {
+        x->pool_node_wanted = -1;
+    }
+    cudaError_t e;
+    {
+        PreferNode scope(x->pool_node_wanted);
+        e = cudaHostAlloc((void**)&x->pool_host, bytes, cudaHostAllocMapped | cudaHostAllocPortable);
+    }
+    if (e == cudaSuccess) {
+        try {
+            sample_placement(x->pool_host, bytes, &x->pool_node_seen, &x->pool_node_frac);
+        } catch (...) {
+            x->pool_node_seen = -1;
+        }
+    }
+    return e;
 }
 
 void free_pool(skv_ctx* x)
@@ -547,6 +732,26 @@ skv_status skv_get_stats(skv_ctx* ctx, uint64_t* calls, uint64_t* hits, uint64_t
     if (calls) *calls = st[skv::STAT_CALLS];
     if (hits) *hits = st[skv::STAT_HITS];
     if (misses) *misses = st[skv::STAT_MISSES];
+    return SKV_OK;
+}
+
+skv_status skv_pool_placement(skv_ctx* ctx, int32_t* wanted_node, int32_t* seen_node, float* seen_frac)
+{
+    if (!ctx) return SKV_ERR_INVALID_ARG;
+    if (wanted_node) *wanted_node = ctx->pool_node_wanted;
+    if (seen_node) *seen_node = ctx->pool_node_seen;
+    if (seen_frac) *seen_frac = ctx->pool_node_frac;
+    return SKV_OK;
+}
+
+skv_status skv_host_node_for_pci(const char* sysfs_root, const char* pci_bus_id, int32_t* node)
+{
+    if (!pci_bus_id || !node) return SKV_ERR_INVALID_ARG;
+    try {  // no C++ exception may leave a C entry point
+        *node = host_node_for_pci(sysfs_root ? sysfs_root : "/sys", sysfs_bus_id(pci_bus_id));
+    } catch (...) {
+        return SKV_ERR_OOM;
+    }
     return SKV_OK;
 }
 

@@ -78,6 +78,8 @@ def _load():
         "skv_selftest_mma": [vp, vp, vp, i32, i32, i32, vp],
         "skv_attend": [vp, vp, i32, i32, vp, vp, vp, vp, ctypes.c_float, vp],
         "skv_selftest_attend_timeout": [vp, vp, i32, vp, vp, vp, vp],
+        "skv_pool_placement": [vp, P(i32), P(i32), P(ctypes.c_float)],
+        "skv_host_node_for_pci": [ctypes.c_char_p, ctypes.c_char_p, P(i32)],
     }
     for name, args in sigs.items():
         f = getattr(lib, name)
@@ -117,8 +119,18 @@ skv_set_attend_sms = lib.skv_set_attend_sms
 skv_selftest_mma = lib.skv_selftest_mma
 skv_attend = lib.skv_attend
 skv_selftest_attend_timeout = lib.skv_selftest_attend_timeout
+skv_pool_placement = lib.skv_pool_placement
+skv_host_node_for_pci = lib.skv_host_node_for_pci
 skv_last_cuda_error = lib.skv_last_cuda_error
 skv_status_string = lib.skv_status_string
+
+
+def host_node_for_pci(pci_bus_id: str, sysfs_root: str | None = None) -> int:
+    """The host NUMA node nearest a PCI device (see skv_host_node_for_pci)."""
+    n = ctypes.c_int32()
+    check(skv_host_node_for_pci(sysfs_root.encode() if sysfs_root else None, pci_bus_id.encode(), ctypes.byref(n)),
+          "skv_host_node_for_pci")
+    return n.value
 
 
 class SkvError(RuntimeError):
@@ -316,6 +328,12 @@ class Context:
         check(skv_get_stats(self.h, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c), _stream_handle(stream)),
               "skv_get_stats")
         return {"calls": a.value, "hits": b.value, "misses": c.value}
+
+    def pool_placement(self):
+        """(wanted node, node holding most sampled pool pages, share there); -1 = none / not reported."""
+        a, b, f = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_float()
+        check(skv_pool_placement(self.h, ctypes.byref(a), ctypes.byref(b), ctypes.byref(f)), "skv_pool_placement")
+        return a.value, b.value, f.value
 
     def set_attend_sms(self, sms: int = 0) -> None:
         """At most `sms` SMs for later attend() calls (0: all; see skv_set_attend_sms)."""

@@ -252,7 +252,7 @@ def check_bruteforce(lib_path=None, T=5, k=2, S_values=(2, 3), steps=3, variant=
 
 def check_invariants(w: wl.Workload, lib_path=None, steps=None):
     """Run workload `w` (small sizes, RB-byte rows) through the oracle and check
-    every invariant after every step."""
+    every invariant after every step; returns the rows the steps gathered."""
     R = w.R
     T_max = w.max_context
     seed = w.base_seed
@@ -269,12 +269,14 @@ def check_invariants(w: wl.Workload, lib_path=None, steps=None):
     gen = wl.TopkStream(w, nthreads=1)
     now = 0
     appended = {}
+    gathered = 0
     nsteps = w.steps if steps is None else steps
     for s in range(nsteps):
         before = {r: o.export(r, tok2slot=False) for r in req_ids}
         topk = gen.step(s, lens)
         err, slots, hits, misses = o.assemble(req_ids, topk)
         assert err == 0
+        gathered += int(misses.sum())
         now += 1
         assert o.now == now
         for b, r in enumerate(req_ids):
@@ -333,6 +335,7 @@ def check_invariants(w: wl.Workload, lib_path=None, steps=None):
                 lens[b] += 1
     o.close()
     gen.close()
+    return gathered
 
 
 # ----------------------------------------------------------------------------

@@ -1,6 +1,8 @@
 """The benchmark's multi-rank harness on CPU (gloo, world size 2): each rank
-runs its own replica with its own seed; elapsed time is the max over ranks and
-work is summed.  No GPU and no data-path collective are involved."""
+runs its own replica with its own seed -- here the CPU oracle over the rank's
+own small workload, every invariant checked after every step -- elapsed time
+is the max over ranks and work is summed.  No GPU and no data-path collective
+are involved."""
 import os
 import socket
 
@@ -26,8 +28,13 @@ def _rank_main(rank, world, port, out):
     w = bench.rank_seed(wl.WORKLOADS["c1_tiny"], r)
     # a replica's input: this rank's first Top-k step
     topk = wl.TopkStream(w, nthreads=1).step(0, [w.ctx] * w.B)
-    elapsed, moved, tokens = bench.reduce_results(dist, 1.0 + r, 100.0 * (r + 1), 10.0)
-    out.put((r, (ws, r, local), w.seed, int(topk.sum()), elapsed, moved, tokens))
+    # the rank's replica, driven on the CPU: the oracle over its own seeded
+    # workload, checked against every invariant after every step
+    import oracle_pins as op
+    small = bench.rank_seed(wl.Workload("replica", B=2, L=2, ctx=600, k=64, S=100, steps=4, fresh=0.3), r)
+    rows = op.check_invariants(small)
+    elapsed, moved, tokens = bench.reduce_results(dist, 1.0 + r, float(rows), 10.0)
+    out.put((r, (ws, r, local), w.seed, int(topk.sum()), elapsed, moved, tokens, rows))
     dist.barrier()
     dist.destroy_process_group()
 
@@ -43,11 +50,12 @@ def test_two_rank_harness_reduces_and_seeds_independently():
     for p in procs:
         p.join(timeout=60)
         assert p.exitcode == 0
-    (r0, env0, seed0, sum0, e0, m0, t0), (r1, env1, seed1, sum1, e1, m1, t1) = res
+    (r0, env0, seed0, sum0, e0, m0, t0, g0), (r1, env1, seed1, sum1, e1, m1, t1, g1) = res
     assert env0 == (2, 0, 0) and env1 == (2, 1, 1)
     assert seed0 != seed1 and sum0 != sum1          # independent replicas
+    assert g0 > 0 and g1 > 0                         # each replica moved rows of its own
     assert e0 == e1 == 2.0                           # max over ranks
-    assert m0 == m1 == 300.0 and t0 == t1 == 20.0    # work summed over ranks
+    assert m0 == m1 == float(g0 + g1) and t0 == t1 == 20.0    # work summed over ranks
 
 
 def test_single_rank_needs_no_process_group():
