@@ -728,8 +728,9 @@ def run_ours(args):
                     "step_miss_rate": M_step / max(tokens, 1.0)}
     if rank == 0:
         achieved = M_step * rb / gather_s / 1e9
-        kname = ("validate_kernel + plan_kernel<fused> (sparse diff + LRU + gather), timed as one pair: the fused "
-                 "kernel is a programmatic dependent launch that runs while validation does")
+        kname = ("validate_kernel + plan_kernel<fused> (sparse diff + LRU + gather), timed as one pair: the events "
+                 "bracket both (with at most one unit per SM the fused kernel starts while validation runs, as a "
+                 "programmatic dependent launch)")
         out = {
             "metric": METRIC,
             "value": bytes_all / elapsed_max / 1e9,
