@@ -706,7 +706,9 @@ def run_ours(args):
                "h2d_bytes_per_step": w.B * 4 + w.B * w.L * w.k * 4,
                "d2h_bytes_per_step": w.B * w.L * w.k * 4 + 2 * w.B * w.L * 4,
                "ms_per_step": 1e3 * e2e_s / len(host_steps), "steps": len(host_steps),
-               "entry_point": "skv_assemble_host (pinned host buffers; copies + sync inside the timed region)"}
+               "entry_point": "skv_assemble_host (pinned host buffers: the Top-k copied in, the slots and counts "
+                              "stored into the pinned outputs by the kernels over the host link; sync inside the "
+                              "timed region)"}
 
     decode_step = None
     if extras:

@@ -271,8 +271,12 @@ SKV_API skv_status skv_prefetch_recent(skv_ctx *ctx, const int32_t *req_ids_dev,
 
 /* skv_assemble for callers whose per-step tensors live in host memory
  * (pinned or pageable): copies req_ids [B] and topk [B][L][k] to device
- * staging buffers owned by the context, runs skv_assemble, copies slots, hits
- * and misses back, and synchronises `stream`.  Same semantics and errors. */
+ * staging buffers owned by the context, runs skv_assemble, and synchronises
+ * `stream`.  An output (slots, hits, misses) in pinned host memory that the
+ * device can address (cudaHostAlloc memory, torch's pin_memory) is written
+ * by the kernels directly, over the host link in the direction the gather
+ * does not use; any other output goes through a device staging buffer and a
+ * copy back.  Same semantics and errors. */
 SKV_API skv_status skv_assemble_host(skv_ctx *ctx, const int32_t *req_ids, int32_t B, const int32_t *topk, int32_t *slots,
                              int32_t *hits, int32_t *misses, skv_stream_t stream);
 

@@ -71,6 +71,19 @@ bool is_device_pointer(const void* p)
 
 void free_pool(skv_ctx* x);
 
+// The device address of host memory the device can write directly (pinned
+// and mapped into its address space, e.g. cudaHostAlloc memory); nullptr for
+// anything else (pageable host memory, device memory).
+void* device_view_of_host(void* p)
+{
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
 void free_ctx(skv_ctx* c)
 {
     if (!c) return;
@@ -632,11 +645,18 @@ skv_status skv_assemble_host(skv_ctx* ctx, const int32_t* req_ids, int32_t B, co
     const size_t entries = units * ctx->cfg.topk;
     SKV_CUDA(cudaMemcpyAsync(ctx->st_req, req_ids, (size_t)B * 4, cudaMemcpyHostToDevice, stream));
     SKV_CUDA(cudaMemcpyAsync(ctx->st_topk, topk, entries * 4, cudaMemcpyHostToDevice, stream));
-    skv_status s = skv_assemble(ctx, ctx->st_req, B, ctx->st_topk, ctx->st_slots, ctx->st_hits, ctx->st_misses, stream);
+    // Outputs in pinned host memory the device can address are written by the kernels themselves,
+    // through the host link in the direction the gather does not use; the others go through the
+    // context's staging buffers and a copy back.
+    int32_t* d_slots = static_cast<int32_t*>(device_view_of_host(slots));
+    int32_t* d_hits = static_cast<int32_t*>(device_view_of_host(hits));
+    int32_t* d_misses = static_cast<int32_t*>(device_view_of_host(misses));
+    skv_status s = skv_assemble(ctx, ctx->st_req, B, ctx->st_topk, d_slots ? d_slots : ctx->st_slots,
+                                d_hits ? d_hits : ctx->st_hits, d_misses ? d_misses : ctx->st_misses, stream);
     if (s != SKV_OK) return s;
-    SKV_CUDA(cudaMemcpyAsync(slots, ctx->st_slots, entries * 4, cudaMemcpyDeviceToHost, stream));
-    SKV_CUDA(cudaMemcpyAsync(hits, ctx->st_hits, units * 4, cudaMemcpyDeviceToHost, stream));
-    SKV_CUDA(cudaMemcpyAsync(misses, ctx->st_misses, units * 4, cudaMemcpyDeviceToHost, stream));
+    if (!d_slots) SKV_CUDA(cudaMemcpyAsync(slots, ctx->st_slots, entries * 4, cudaMemcpyDeviceToHost, stream));
+    if (!d_hits) SKV_CUDA(cudaMemcpyAsync(hits, ctx->st_hits, units * 4, cudaMemcpyDeviceToHost, stream));
+    if (!d_misses) SKV_CUDA(cudaMemcpyAsync(misses, ctx->st_misses, units * 4, cudaMemcpyDeviceToHost, stream));
     SKV_CUDA(cudaStreamSynchronize(stream));
     return SKV_OK;
 }

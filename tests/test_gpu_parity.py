@@ -114,18 +114,29 @@ def test_graph_capture_replays_the_step():
         p.close()
 
 
-def test_host_buffer_entry_point():
-    """skv_assemble_host (host-memory inputs and outputs) matches the oracle."""
+@pytest.mark.parametrize("outputs", ["pageable", "pinned", "mixed"])
+def test_host_buffer_entry_point(outputs):
+    """skv_assemble_host (host-memory inputs and outputs) matches the oracle,
+    whether its outputs are pageable (staged and copied back), pinned (written
+    by the kernels straight into host memory) or some of each."""
     w = wl.Workload("host", B=3, L=2, ctx=3000, k=300, S=512, steps=8, fresh=0.3)
     p = Pair(w)
+
+    def out(shape, pinned):
+        if not pinned:
+            return np.full(shape, -7, np.int32)
+        return torch.full(shape, -7, dtype=torch.int32).pin_memory()
+
     try:
         for s in range(w.steps):
             topk = p.gen.step(s, p.lens)
             req = np.array(p.req_ids, dtype=np.int32)
-            slots = np.empty_like(topk)
-            hits = np.empty((w.B, w.L), np.int32)
-            misses = np.empty((w.B, w.L), np.int32)
+            slots = out(topk.shape, outputs != "pageable")
+            hits = out((w.B, w.L), outputs == "pinned")
+            misses = out((w.B, w.L), outputs != "pageable")
             p.ctx.assemble_host(req, topk, slots, hits, misses)
+            slots, hits, misses = (np.asarray(x) if isinstance(x, np.ndarray) else x.numpy()
+                                   for x in (slots, hits, misses))
             e, o_slots, o_hits, o_misses = p.orc.assemble(p.req_ids, topk)
             assert e == 0
             assert np.array_equal(slots, o_slots) and np.array_equal(hits, o_hits)
