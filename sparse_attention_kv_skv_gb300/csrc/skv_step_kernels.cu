@@ -44,14 +44,6 @@ struct PlanSync {
                      : "=r"(r) : "r"((uint32_t)p), "r"(n) : "memory");
         return r != 0;
     }
-    __device__ __forceinline__ bool all(bool p) const
-    {
-        if (!kNamed) return __syncthreads_and(p) != 0;
-        uint32_t r;
-        asm volatile("{\n .reg .pred q, o;\n setp.ne.u32 q, %1, 0;\n bar.red.and.pred o, 1, %2, q;\n selp.u32 %0, 1, 0, o;\n}\n"
-                     : "=r"(r) : "r"((uint32_t)p), "r"(n) : "memory");
-        return r != 0;
-    }
 };
 using CtaSync = PlanSync<false>;
 
