@@ -249,7 +249,7 @@ def hbm_peak_gbs():
 # dram__bytes_read.sum + dram__bytes_write.sum.  Valid only while the kernel
 # source is the one that was captured; scaled to other workloads by units.
 PROFILED_TRAFFIC = {"source": "sparse_attention_kv_skv_gb300/csrc/skv_step_kernels.cu",
-                    "sha256": "77ea5d673cac3fe5ae03ba3855c1bca7b2030c1b0f0d770112234e1089528878",
+                    "sha256": "19042200e8b989adeb0ce9727c08e7e24af98da6e43702b2e3ea6edb4a6b21b1",
                     "units": 512, "dram_bytes": 42.495488e6 + 195.300608e6}
 
 
