@@ -50,6 +50,7 @@ sys.path.insert(0, ROOT)
 import skv_workload as wl  # noqa: E402
 
 METRIC = "missed-KV GB/s per skv_assemble step (host pool -> HBM hot buffer)"
+L2_BYTES = 126 << 20  # GB300's L2
 DEFAULT_WORKLOAD = "target_16k_b192_f20"
 
 
@@ -82,8 +83,9 @@ def parse():
                          "step's slots (`attention`), then as many pipelined decode steps (`decode_step`); 0: none")
     ap.add_argument("--decode-attend-sms", type=int, default=96,
                     help="SMs the attention may occupy in the pipelined decode step")
-    ap.add_argument("--cpu-sample-requests", type=int, default=32)
-    ap.add_argument("--cpu-sample-steps", type=int, default=24)
+    ap.add_argument("--cpu-sample-requests", type=int, default=0,
+                    help="requests of the workload the CPU oracle runs (0: all of them)")
+    ap.add_argument("--cpu-sample-steps", type=int, default=12)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     return ap.parse_args()
@@ -261,6 +263,19 @@ def profiled_traffic(w: wl.Workload):
     return PROFILED_TRAFFIC["dram_bytes"] * (w.B * w.L) / PROFILED_TRAFFIC["units"]
 
 
+def workload_config(w: wl.Workload) -> dict:
+    """The workload, as both arms name it in `config` (the same dict, so that
+    the two lines can be compared): its shape, and how the timed steps relate
+    to L2."""
+    return {"workload": w.name, "batch": w.B, "layers": w.L, "context": w.ctx, "topk": w.k, "hot_slots": w.S,
+            "fresh": w.fresh, "row_bytes": wl.ROW_BYTES, "row_dtype": "bf16", "write_back_per_step": w.appends,
+            "turn_every": w.turn_every, "turn_tokens": w.turn_tokens,
+            "l2": (f"inputs larger than L2 ({L2_BYTES / 1e6:.0f} MB): each step writes the missed rows into a "
+                   f"{w.hot_bytes() / 1e9:.2f} GB hot buffer and reads {w.B * w.L * w.max_context * 4 / 1e6:.0f} MB "
+                   "of token->slot maps; no flush") if w.hot_bytes() + w.B * w.L * w.max_context * 4 > L2_BYTES else
+                  f"footprint smaller than L2 ({L2_BYTES / 1e6:.0f} MB): a parity configuration, not a bench workload"}
+
+
 def hbm_algorithmic_bytes(w: wl.Workload, M: int, hits: int) -> int:
     """Bytes one step must move in HBM (besides the link reads): Top-k read,
     tok2slot probes, slot tensor write, LRU order read+write, clock stamps of
@@ -272,11 +287,12 @@ def hbm_algorithmic_bytes(w: wl.Workload, M: int, hits: int) -> int:
 def cpu_baseline(w: wl.Workload, pool_addr: int | None, n_req: int, n_steps: int, warm: int = 2,
                  one_core_steps: int = 0):
     """The oracle as it stands, on this host's cores, over the first n_req
-    requests of the workload for n_steps steady-state steps (after `warm`
-    steps, the first of which is cold); then, if one_core_steps > 0, that many
-    further steps on one core.  Returns (GB/s, tokens/s, info)."""
+    requests of the workload (all of them for n_req <= 0) for n_steps
+    steady-state steps (after `warm` steps, the first of which is cold); then,
+    if one_core_steps > 0, that many further steps on one core.  Returns
+    (GB/s, tokens/s, info)."""
     import oracle as orc
-    n_req = min(n_req, w.B)
+    n_req = w.B if n_req <= 0 else min(n_req, w.B)
     T_max = w.max_context
     rb = wl.ROW_BYTES
     own = None
@@ -719,7 +735,7 @@ def run_ours(args):
     elapsed_max, bytes_all, tokens_all = reduce_results(dist, elapsed, float(M * rb), tokens)
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        gbs, tps, info = cpu_baseline(w, pool, args.cpu_sample_requests, args.cpu_sample_steps, one_core_steps=2)
+        gbs, tps, info = cpu_baseline(w, pool, args.cpu_sample_requests, args.cpu_sample_steps, one_core_steps=1)
         cpu = {"value": gbs, "unit": "GB/s", "cores": info["cores"], "kind": "oracle", "sample": info["sample"],
                "assembled_tokens_per_s": tps, "one_core": info["one_core"]}
     prefetch = None
@@ -746,15 +762,9 @@ def run_ours(args):
             "vs_baseline": None,
             "dtype": "int32",
             "data": "synthetic",
-            "config": {"workload": w.name, "batch": w.B, "layers": w.L, "context": w.ctx, "topk": w.k,
-                       "hot_slots": w.S, "fresh": w.fresh, "row_bytes": rb, "row_dtype": "bf16",
-                       "write_back_per_step": w.appends, "cuda_graph": use_graph, "graphs_uploaded": uploaded,
-                       "layered": layered, "turn_every": w.turn_every, "turn_tokens": w.turn_tokens,
-                       "attend": attn_on, "pipeline": bool(args.pipeline), "attend_sms": args.attend_sms,
-                       "prefetch_window": pf,
-                       "l2": "inputs larger than L2: each step writes the missed rows (~0.6 GB) into a "
-                             f"{w.hot_bytes() / 1e9:.2f} GB hot buffer and reads {w.B * w.L * w.max_context * 4 / 1e6:.0f} MB "
-                             "of token->slot maps; no flush"},
+            "config": workload_config(w),
+            "run": {"cuda_graph": use_graph, "graphs_uploaded": uploaded, "layered": layered, "attend": attn_on,
+                    "pipeline": bool(args.pipeline), "attend_sms": args.attend_sms, "prefetch_window": pf},
             "assembled_tokens_per_s": tokens_all / elapsed_max,
             "miss_rate": M_step / max(tokens, 1.0),
             "missed_rows_per_step": M / K,
@@ -823,14 +833,13 @@ def run_reference(args):
         "vs_baseline": None,
         "dtype": "int32",
         "data": "synthetic",
-        "config": {"workload": w.name, "batch": w.B, "layers": w.L, "context": w.ctx, "topk": w.k,
-                   "hot_slots": w.S, "fresh": w.fresh, "row_bytes": wl.ROW_BYTES},
+        "config": workload_config(w),
         "assembled_tokens_per_s": tps,
         "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": info["cores"], "kind": "oracle",
                          "sample": info["sample"]},
         "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "note": "the reference pages ship no code; this arm times the CPU oracle (plain C++ hash map + LRU "
-                "list + memcpy) on a bounded sample of the same workload",
+                "list + memcpy) on the same workload, all of its requests",
     }
     print(json.dumps(out), flush=True)
 
