@@ -50,7 +50,7 @@ sys.path.insert(0, ROOT)
 import skv_workload as wl  # noqa: E402
 
 METRIC = "missed-KV GB/s per skv_assemble step (host pool -> HBM hot buffer)"
-L2_BYTES = 126 << 20  # GB300's L2
+L2_BYTES = 129_000_000  # GB300's L2
 DEFAULT_WORKLOAD = "target_16k_b192_f20"
 
 
