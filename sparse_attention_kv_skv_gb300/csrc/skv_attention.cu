@@ -529,14 +529,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
                 tc::tmem_wait_st();
                 tc::fence_before_sync();
                 tc::mbar_arrive(&c.q_ready);
-                if (u + ncl < units) {  // warm L2 with the next unit's Q row
+            }
+            for (int i = 0; ok && i < nblk; ++i) {
+                const int g = g0 + i;
+                // warm L2 with the next unit's Q row a few blocks before it is loaded (earlier, the key rows
+                // streaming through L2 in the meantime would evict it)
+                if (i == (nblk > 3 ? nblk - 3 : 0) && u + ncl < units) {
                     const uint8_t* nq = reinterpret_cast<const uint8_t*>(q + ((size_t)(u + ncl) * kHeads + hd) * kDim + h * kQKHalf);
 #pragma unroll
                     for (int x = 0; x < 5; ++x) tc::prefetch_l2(nq + 128 * x);
                 }
-            }
-            for (int i = 0; ok && i < nblk; ++i) {
-                const int g = g0 + i;
                 if (g >= 2 && !(ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.adv[g & 1], (uint32_t)((g - 2) >> 1) & 1u, abort))))
                     break;
                 if (!(ok = __all_sync(0xFFFFFFFFu, wait_phase(&c.s_full, (uint32_t)g & 1u, abort)))) break;
