@@ -56,6 +56,25 @@ def test_ragged_and_edge_workloads(w):
     run(w)
 
 
+@pytest.mark.parametrize("B,L", [(38, 4), (50, 6), (60, 9)], ids=["152_units", "300_units", "540_units"])
+def test_launch_regimes_by_unit_count(B, L):
+    """The fused kernel's three launch regimes: at most one unit per SM (a
+    prefetch warp, the kernel starting while validation runs), more units than
+    SMs but all resident at once (in-line L2 prefetch), and more than fit at
+    once (units in waves) -- each bit-exact against the oracle, with state
+    compared at the end."""
+    w = wl.Workload(f"regime_{B * L}", B=B, L=L, ctx=2500, k=192, S=320, steps=4, fresh=0.3,
+                    order=wl.ORDER_SHUFFLED, n_pad=5)
+    p = Pair(w)
+    try:
+        for s in range(w.steps):
+            p.step(s)
+        p.compare_state(reqs=[0, B // 2, B - 1])
+        assert p.ctx.get_device_error() == 0
+    finally:
+        p.close()
+
+
 def test_request_ids_permuted_and_sparse():
     """R > B: the batch uses a permuted subset of the published requests."""
     w = wl.Workload("perm", B=4, L=2, ctx=3000, k=200, S=400, steps=10, fresh=0.3, max_requests=7)
