@@ -20,7 +20,8 @@ same context runs on: ``attention`` times skv_attend over each further step's
 slots (CUDA events around the call; TFLOP/s against the measured bf16 peaks),
 and ``decode_step`` times the layer-pipelined decode step (per layer
 skv_assemble_layer, then that layer's skv_attend on a second stream limited to
-``--decode-attend-sms`` SMs beside the next layer's assembly; graph replays).
+``--decode-attend-sms`` SMs beside the next layer's assembly, the last layer's
+on every SM; graph replays).
 Neither changes ``value`` or ``ms_per_step``.
 
 Variants of the step (reported under their own keys, same metric):
@@ -29,7 +30,8 @@ Variants of the step (reported under their own keys, same metric):
                       each assemble call (``prefetch``: rows it moved, the step's misses)
   --attend            skv_attend over each step's slots (``attention``: ms, TFLOP/s)
   --pipeline          with --layered --attend: layer l's attention on its own stream
-                      beside layer l+1's assembly; --attend-sms caps its SMs
+                      beside layer l+1's assembly; --attend-sms caps its SMs (not
+                      the last layer's, which runs alone)
 """
 from __future__ import annotations
 
@@ -81,7 +83,7 @@ def parse():
     ap.add_argument("--extra-steps", type=int, default=12,
                     help="after the headline region (plain step only): this many steps with skv_attend over each "
                          "step's slots (`attention`), then as many pipelined decode steps (`decode_step`); 0: none")
-    ap.add_argument("--decode-attend-sms", type=int, default=96,
+    ap.add_argument("--decode-attend-sms", type=int, default=72,
                     help="SMs the attention may occupy in the pipelined decode step")
     ap.add_argument("--cpu-sample-requests", type=int, default=0,
                     help="requests of the workload the CPU oracle runs (0: all of them)")
@@ -357,8 +359,8 @@ def run_extras(torch, ctx, w: wl.Workload, dev, stream, req, att_topk, dec_topk,
     first two calls are warm-up); (2) the decode step of F1 + F4: per layer,
     skv_assemble_layer on the main stream and, as soon as it is done, that
     layer's skv_attend on a second stream limited to `attend_sms` SMs, beside
-    the next layer's assembly; each step one CUDA graph replay after two
-    warm-up steps."""
+    the next layer's assembly (the last layer's, with nothing beside it, on
+    every SM); each step one CUDA graph replay after two warm-up steps."""
     B, L, k = w.B, w.L, w.k
     units = B * L
     flops_per_entry = 2.0 * 128 * (576 + 512)  # q.k over 576 dims and p.v over 512, 128 heads
@@ -417,7 +419,10 @@ def run_extras(torch, ctx, w: wl.Workload, dev, stream, req, att_topk, dec_topk,
                                stream=stream.cuda_stream)
             ev_layer[l].record(stream)
             side.wait_event(ev_layer[l])
+            # the last layer's attention has the GPU to itself: no assembly runs beside it
+            ctx.set_attend_sms(0 if l == L - 1 else attend_sms)
             ctx.attend(req, q_l[l], slots_l[l], out_l[l], lse_l[l], layer=l, stream=side.cuda_stream)
+        ctx.set_attend_sms(attend_sms)
         ev_join.record(side)
         stream.wait_event(ev_join)
 
@@ -458,7 +463,8 @@ def run_extras(torch, ctx, w: wl.Workload, dev, stream, req, att_topk, dec_topk,
                    "assembled_tokens_per_s": entries / dec_s,
                    "attention_tflops": entries * flops_per_entry / dec_s / 1e12,
                    "what": "per layer: skv_assemble_layer on the main stream, then that layer's skv_attend on a "
-                           "second stream (at most attend_sms SMs) beside the next layer's assembly; one CUDA "
+                           "second stream (at most attend_sms SMs) beside the next layer's assembly, the last "
+                           "layer's on every SM; one CUDA "
                            f"graph replay per step, {warm_d} warm-up steps (the first eager)",
                    "warmup_calls_ok": st1["calls"] - st0["calls"] == warm_d * L}
     return attention, decode_step
@@ -594,8 +600,11 @@ def run_ours(args):
                     if args.pipeline:
                         ev_layer[l].record(stream)
                         side.wait_event(ev_layer[l])
+                        # the last layer's attention has nothing beside it: every SM
+                        ctx.set_attend_sms(0 if l == w.L - 1 else args.attend_sms)
                     ctx.attend(req, q_all[l], slots[l], att_out[l], att_lse[l], layer=l, stream=astream.cuda_stream)
             if args.pipeline:
+                ctx.set_attend_sms(args.attend_sms)
                 ev_join.record(side)
                 stream.wait_event(ev_join)
         else:
