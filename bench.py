@@ -253,8 +253,8 @@ def hbm_peak_gbs():
 # dram__bytes_read.sum + dram__bytes_write.sum.  Valid only while the kernel
 # source is the one that was captured; scaled to other workloads by units.
 PROFILED_TRAFFIC = {"source": "sparse_attention_kv_skv_gb300/csrc/skv_step_kernels.cu",
-                    "sha256": "19042200e8b989adeb0ce9727c08e7e24af98da6e43702b2e3ea6edb4a6b21b1",
-                    "units": 512, "dram_bytes": 42.495488e6 + 195.300608e6}
+                    "sha256": "288cfbb5008ef18f9ba7922a2e1e33739db3638d7c6baa35c79ab0a0e4244d8e",
+                    "units": 512, "dram_bytes": 42.512384e6 + 194.361088e6}
 
 
 def profiled_traffic(w: wl.Workload):

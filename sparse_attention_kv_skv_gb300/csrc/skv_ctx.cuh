@@ -21,7 +21,6 @@ struct skv_ctx {
     uint32_t* host_word = nullptr;  // pinned word for reading the error bits
     cudaEvent_t ev_before = nullptr, ev_after = nullptr;
     int gather_grid = 0;
-    int plan_resident = 1;  // fused-kernel CTAs resident at once (L2 prefetch budget)
     CUtensorMap hot_map{};  // TMA view of the hot buffer for the attention consumer (built on first use)
     bool hot_map_ready = false;
     int attend_sms = 0;     // SMs the attention kernel may occupy (0: all)

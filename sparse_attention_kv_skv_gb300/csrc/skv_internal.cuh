@@ -61,21 +61,18 @@ size_t validate_smem_bytes(int k);
 
 // Step kernels (assemble).
 cudaError_t launch_validate(const Dev& d, const int32_t* req_ids, int B, const int32_t* topk, cudaStream_t st);
-// plan with a global work list (copied by launch_gather); prefetch_rows > 0
-// prefetches up to that many missing rows per unit into L2; pdl lets it start
+// plan with a global work list (copied by launch_gather); pdl lets it start
 // while validate runs.
 cudaError_t launch_plan(const Dev& d, const int32_t* req_ids, int B, const int32_t* topk, int32_t* slots,
-                        int32_t* hits, int32_t* misses, int prefetch_rows, bool pdl, cudaStream_t st);
-constexpr size_t kPrefetchBudgetBytes = (size_t)64 << 20;  // L2 share for prefetched rows
+                        int32_t* hits, int32_t* misses, bool pdl, cudaStream_t st);
+constexpr size_t kPrefetchBudgetBytes = (size_t)64 << 20;  // L2 share for rows the prefetch warps pull
 cudaError_t launch_gather(const Dev& d, int grid, cudaStream_t st);
 // plan + gather fused: each (b, l) CTA copies its own misses right after
 // planning them; the last CTA to finish commits the call.
 // device_sms: the device's SM count (at most that many units: one CTA per SM
-// with more loads in flight per thread).
+// with a prefetch warp and more loads in flight per thread).
 cudaError_t launch_plan_gather(const Dev& d, const int32_t* req_ids, int B, const int32_t* topk, int32_t* slots,
-                               int32_t* hits, int32_t* misses, int resident_ctas, int device_sms, cudaStream_t st);
-// CTAs of the fused kernel that fit on the device at once for (k, S).
-int plan_resident_ctas(int k, int S);
+                               int32_t* hits, int32_t* misses, int device_sms, cudaStream_t st);
 cudaError_t prepare_step_kernels(int k, int S, int* gather_grid);
 
 // Attention over assembled slots (tensor cores).

@@ -101,7 +101,7 @@ extern "C" skv_status skv_assemble_noalloc(skv_ctx* ctx, const int32_t* req_ids_
         skv::Dev d = ctx->d;  // the context's state, with the static work list
         d.jobs = jobs;
         if ((e = skv::launch_validate(d, req_ids_dev, B, topk_dev, stream)) != cudaSuccess ||
-            (e = skv::launch_plan(d, req_ids_dev, B, topk_dev, slots_dev, hits_dev, misses_dev, 0, false, stream)) !=
+            (e = skv::launch_plan(d, req_ids_dev, B, topk_dev, slots_dev, hits_dev, misses_dev, false, stream)) !=
                 cudaSuccess ||
             (e = skv::launch_gather(d, ctx->gather_grid, stream)) != cudaSuccess)
             st = fail(std::string("skv_assemble_noalloc: kernel launch: ") + cudaGetErrorString(e), SKV_ERR_CUDA);

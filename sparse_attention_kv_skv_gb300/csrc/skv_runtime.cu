@@ -461,7 +461,6 @@ skv_status skv_create(const skv_config* cfg, skv_ctx** out)
     SKV_TRY(cudaMemset(d.stats, 0, skv::STAT_WORDS * 8));
     SKV_TRY(skv::launch_init_lru_all(d, 0));
     SKV_TRY(skv::prepare_step_kernels(c.topk, c.hot_slots, &x->gather_grid));
-    x->plan_resident = skv::plan_resident_ctas(c.topk, c.hot_slots);
     SKV_TRY(skv::prepare_attend(&x->device_sms));
     SKV_TRY(skv::noalloc_prepare(c.device));
     SKV_TRY(cudaDeviceSynchronize());
@@ -553,8 +552,8 @@ skv_status assemble_impl(skv_ctx* ctx, const Dev& d, const int32_t* req_ids_dev,
 {
     if (timed && ctx->ev_before) SKV_CUDA(record_event(ctx->ev_before, stream));
     SKV_CUDA(skv::launch_validate(d, req_ids_dev, B, topk_dev, stream));
-    SKV_CUDA(skv::launch_plan_gather(d, req_ids_dev, B, topk_dev, slots_dev, hits_dev, misses_dev, ctx->plan_resident,
-                                     ctx->device_sms, stream));
+    SKV_CUDA(skv::launch_plan_gather(d, req_ids_dev, B, topk_dev, slots_dev, hits_dev, misses_dev, ctx->device_sms,
+                                     stream));
     if (timed && ctx->ev_after) SKV_CUDA(record_event(ctx->ev_after, stream));
     return SKV_OK;
 }

@@ -316,12 +316,12 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes)
 // and works in shared memory, so it may run before validation has finished:
 // indices are bounds-checked against the allocation (not against len) before
 // any load, and nothing global is written until pdl_wait() has returned and
-// the call is known to be accepted.  `prefetch_rows` caps how many of this
-// unit's missing rows are prefetched into L2 as soon as they are known (a
-// budget so that all resident CTAs' prefetches fit in L2).
+// the call is known to be accepted.
 //
-// kPfWarp: the CTA has a seventeenth warp that issues those
-// prefetches.  A bulk prefetch instruction waits while the link is busy (up to
+// kPfWarp: the CTA has a seventeenth warp that prefetches the unit's missing
+// rows into L2 as soon as they are known, at most `prefetch_rows` of them (a
+// budget so that all CTAs' prefetches fit in L2; unused without the warp).
+// A bulk prefetch instruction waits while the link is busy (up to
 // tens of microseconds for a few hundred rows per SM), so planning threads
 // that issued them themselves stood still; the prefetch warp takes the sorted
 // miss list through named barrier 2 and the kPlanThreads planning threads
@@ -415,10 +415,6 @@ __global__ void __launch_bounds__(kPfWarp ? kPlanThreads + 32 : kPlanThreads, MI
                 sm.out[i] = -2;
                 missmask |= 1u << j;
                 ++nmiss;
-                // the budget covers every possible miss of this unit: start
-                // pulling the row over the host link right away
-                if (!kPfWarp && prefetch_rows >= k)
-                    prefetch_l2(d.pool + ((size_t)u * d.T_max + t) * d.row_bytes, (uint32_t)d.row_bytes);
             }
         }
         uint32_t total;
@@ -458,16 +454,11 @@ __global__ void __launch_bounds__(kPfWarp ? kPlanThreads + 32 : kPlanThreads, MI
             }
         }
 
-        // the missing rows are known: start pulling (the first) of them over
-        // the host link while the LRU work below runs
+        // the missing rows are known: the prefetch warp starts pulling (the
+        // first) of them over the host link while the LRU work below runs
         if (kPfWarp) {
             if (tid == 0) pf_count_sh = (uint32_t)(m < prefetch_rows ? m : prefetch_rows);
             asm volatile("bar.arrive 2, %0;" ::"r"(NT + 32) : "memory");
-        } else if (prefetch_rows < k) {  // otherwise every row was prefetched in phase A
-            const int npf = m < prefetch_rows ? m : prefetch_rows;
-            const uint8_t* src = d.pool + (size_t)u * d.T_max * d.row_bytes;
-            for (int j = tid; j < npf; j += NT)
-                prefetch_l2(src + (size_t)(sm.miss[j] >> 32) * d.row_bytes, (uint32_t)d.row_bytes);
         }
 
         // C. victims: the first m non-hit slots in LRU order
@@ -705,7 +696,7 @@ cudaError_t launch_validate(const Dev& d, const int32_t* req_ids, int B, const i
 }
 
 cudaError_t launch_plan(const Dev& d, const int32_t* req_ids, int B, const int32_t* topk, int32_t* slots,
-                        int32_t* hits, int32_t* misses, int prefetch_rows, bool pdl, cudaStream_t st)
+                        int32_t* hits, int32_t* misses, bool pdl, cudaStream_t st)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(call_units(d, B));
@@ -717,20 +708,21 @@ cudaError_t launch_plan(const Dev& d, const int32_t* req_ids, int B, const int32
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, plan_kernel<false, 0>, d, req_ids, topk, slots, hits, misses, prefetch_rows);
+    return cudaLaunchKernelEx(&cfg, plan_kernel<false, 0>, d, req_ids, topk, slots, hits, misses, 0);
 }
 
 cudaError_t launch_plan_gather(const Dev& d, const int32_t* req_ids, int B, const int32_t* topk, int32_t* slots,
-                               int32_t* hits, int32_t* misses, int resident_ctas, int device_sms, cudaStream_t st)
+                               int32_t* hits, int32_t* misses, int device_sms, cudaStream_t st)
 {
-    // L2 prefetch of the missing rows pays only when every CTA is resident at
-    // once (few units: planning is otherwise exposed); with more units than
-    // fit, the link is already kept busy by other CTAs and the prefetched
-    // lines compete with the streaming gather (measured: -1.5 % to -4 %)
+    // few units (at most one per SM): the variant with a prefetch warp and more
+    // loads in flight per thread.  L2 prefetch of the missing rows pays only
+    // there (planning is otherwise exposed); with more units the link is kept
+    // busy by other CTAs and the prefetched lines compete with the streaming
+    // gather: measured -1.5 % to -4 % for units in waves, and 3.22 against
+    // 3.12 ms a step for eight layer calls of 192 co-resident units.
     const int grid = call_units(d, B);
-    const int prefetch_rows = grid <= resident_ctas ? (int)((kPrefetchBudgetBytes / d.row_bytes) / grid) : 0;
-    // few units (at most one per SM): the variant with a prefetch warp and more loads in flight per thread
     const bool few = grid <= device_sms;
+    const int prefetch_rows = few ? (int)((kPrefetchBudgetBytes / d.row_bytes) / grid) : 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(few ? kPlanThreads + 32 : kPlanThreads);
@@ -755,17 +747,6 @@ cudaError_t launch_plan_gather(const Dev& d, const int32_t* req_ids, int B, cons
     return few ? cudaLaunchKernelEx(&cfg, plan_kernel<true, 0, kFewUnitsUnroll, 1, true>, d, req_ids, topk, slots, hits,
                                     misses, prefetch_rows)
                : cudaLaunchKernelEx(&cfg, plan_kernel<true, 0>, d, req_ids, topk, slots, hits, misses, prefetch_rows);
-}
-
-int plan_resident_ctas(int k, int S)
-{
-    int dev = 0, sms = 0, per_sm = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 1;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, plan_kernel<true, 72>, kPlanThreads,
-                                                      plan_smem_bytes(k, S)) != cudaSuccess)
-        return 1;
-    return sms * (per_sm > 0 ? per_sm : 1);
 }
 
 cudaError_t launch_gather(const Dev& d, int grid, cudaStream_t st)
