@@ -253,8 +253,8 @@ def hbm_peak_gbs():
 # dram__bytes_read.sum + dram__bytes_write.sum.  Valid only while the kernel
 # source is the one that was captured; scaled to other workloads by units.
 PROFILED_TRAFFIC = {"source": "sparse_attention_kv_skv_gb300/csrc/skv_step_kernels.cu",
-                    "sha256": "288cfbb5008ef18f9ba7922a2e1e33739db3638d7c6baa35c79ab0a0e4244d8e",
-                    "units": 512, "dram_bytes": 42.512384e6 + 194.361088e6}
+                    "sha256": "eed49c1d4efef205528b57a6de76526069b7a967d464dc9ac30ded9040a642c2",
+                    "units": 512, "dram_bytes": 42.48064e6 + 194.504192e6}
 
 
 def profiled_traffic(w: wl.Workload):

@@ -65,12 +65,11 @@ cudaError_t launch_validate(const Dev& d, const int32_t* req_ids, int B, const i
 // while validate runs.
 cudaError_t launch_plan(const Dev& d, const int32_t* req_ids, int B, const int32_t* topk, int32_t* slots,
                         int32_t* hits, int32_t* misses, bool pdl, cudaStream_t st);
-constexpr size_t kPrefetchBudgetBytes = (size_t)64 << 20;  // L2 share for rows the prefetch warps pull
 cudaError_t launch_gather(const Dev& d, int grid, cudaStream_t st);
 // plan + gather fused: each (b, l) CTA copies its own misses right after
 // planning them; the last CTA to finish commits the call.
 // device_sms: the device's SM count (at most that many units: one CTA per SM
-// with a prefetch warp and more loads in flight per thread).
+// with more loads in flight per thread).
 cudaError_t launch_plan_gather(const Dev& d, const int32_t* req_ids, int B, const int32_t* topk, int32_t* slots,
                                int32_t* hits, int32_t* misses, int device_sms, cudaStream_t st);
 cudaError_t prepare_step_kernels(int k, int S, int* gather_grid);

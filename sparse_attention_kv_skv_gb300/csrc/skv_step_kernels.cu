@@ -22,30 +22,13 @@ constexpr uint32_t kEmpty = 0xFFFFFFFFu;
 constexpr int kMaxIpt = kMaxTopk / kPlanThreads;  // Top-k entries per plan thread
 
 // ---------------------------------------------------------------------------
-// The threads that plan, and how they synchronise: the whole CTA
-// (__syncthreads), or -- when the CTA has a prefetch warp that must not be held
-// up -- the first n threads on named barrier 1.
+// The CTA's threads and how they synchronise (__syncthreads).
 // ---------------------------------------------------------------------------
-template <bool kNamed>
-struct PlanSync {
-    int n;  // planning threads: blockDim.x, or the first n (a multiple of 32)
-    __device__ __forceinline__ void sync() const
-    {
-        if (kNamed)
-            asm volatile("bar.sync 1, %0;" ::"r"(n) : "memory");
-        else
-            __syncthreads();
-    }
-    __device__ __forceinline__ bool any(bool p) const
-    {
-        if (!kNamed) return __syncthreads_or(p) != 0;
-        uint32_t r;
-        asm volatile("{\n .reg .pred q, o;\n setp.ne.u32 q, %1, 0;\n bar.red.or.pred o, 1, %2, q;\n selp.u32 %0, 1, 0, o;\n}\n"
-                     : "=r"(r) : "r"((uint32_t)p), "r"(n) : "memory");
-        return r != 0;
-    }
+struct CtaSync {
+    int n;  // blockDim.x (a multiple of 32)
+    __device__ __forceinline__ void sync() const { __syncthreads(); }
+    __device__ __forceinline__ bool any(bool p) const { return __syncthreads_or(p) != 0; }
 };
-using CtaSync = PlanSync<false>;
 
 // ---------------------------------------------------------------------------
 // block-wide exclusive prefix sum over the syncing threads (a multiple of 32,
@@ -294,16 +277,9 @@ __device__ __forceinline__ void finish_call(const Dev& d)
 // unit has an SM to itself (few units: each CTA must cover the link latency
 // alone; a bare gather of 16 units x 410 scattered rows took 67 us with 4
 // loads in flight a thread and 45 us with 16 or with the rows prefetched into
-// L2 first, as the prefetch warp does).
+// L2 first).
 constexpr int kFusedUnroll = 4;
 constexpr int kFewUnitsUnroll = 8;
-
-// Fetch `bytes` (multiple of 16, 16-byte aligned) at a global address into L2
-// without waiting for it.
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
 
 // kFused = false: the misses become jobs of the global work list, copied by
 // gather_kernel.  kFused = true: the CTA copies its own misses (pool row ->
@@ -318,29 +294,18 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes)
 // any load, and nothing global is written until pdl_wait() has returned and
 // the call is known to be accepted.
 //
-// kPfWarp: the CTA has a seventeenth warp that prefetches the unit's missing
-// rows into L2 as soon as they are known, at most `prefetch_rows` of them (a
-// budget so that all CTAs' prefetches fit in L2; unused without the warp).
-// A bulk prefetch instruction waits while the link is busy (up to
-// tens of microseconds for a few hundred rows per SM), so planning threads
-// that issued them themselves stood still; the prefetch warp takes the sorted
-// miss list through named barrier 2 and the kPlanThreads planning threads
-// synchronise among themselves on named barrier 1, so planning, map updates
-// and the gather run on while the prefetches queue.  The whole CTA meets only
-// at the end (finish_call).
-template <bool kFused, int CPR_CONST, int UNR = kFusedUnroll, int MINB = 3, bool kPfWarp = false>
-__global__ void __launch_bounds__(kPfWarp ? kPlanThreads + 32 : kPlanThreads, MINB)
+// UNR: 16-byte loads in flight per thread in the gather; MINB: CTAs per SM the
+// register budget is sized for (3 when units run in waves, 1 for few units).
+template <bool kFused, int CPR_CONST, int UNR = kFusedUnroll, int MINB = 3>
+__global__ void __launch_bounds__(kPlanThreads, MINB)
     plan_kernel(Dev d, const int32_t* __restrict__ req_ids, const int32_t* __restrict__ topk,
-                int32_t* __restrict__ slots_out, int32_t* __restrict__ hits_out, int32_t* __restrict__ misses_out,
-                int prefetch_rows)
+                int32_t* __restrict__ slots_out, int32_t* __restrict__ hits_out, int32_t* __restrict__ misses_out)
 {
-    static_assert(!kPfWarp || kFused, "the prefetch warp belongs to the fused kernel");
     extern __shared__ __align__(16) uint8_t smem_raw[];
     __shared__ uint32_t scan_sh[32];
     __shared__ uint32_t job_base_sh;
-    __shared__ uint32_t pf_count_sh;  // rows the prefetch warp pulls into L2
-    const int tid = threadIdx.x, NT = kPfWarp ? (int)blockDim.x - 32 : (int)blockDim.x;  // NT planning threads
-    const PlanSync<kPfWarp> sy{NT};
+    const int tid = threadIdx.x, NT = (int)blockDim.x;
+    const CtaSync sy{NT};
     const int k = d.k, S = d.S;
     const int cpr = CPR_CONST > 0 ? CPR_CONST : d.row_bytes / 16;
     const int32_t* row = topk + (size_t)blockIdx.x * k;
@@ -360,19 +325,6 @@ __global__ void __launch_bounds__(kPfWarp ? kPlanThreads + 32 : kPlanThreads, MI
     const int ipt = (k + NT - 1) / NT;
     const int i0 = tid * ipt;
     int m = 0, h = 0;
-
-    if (kPfWarp && tid >= NT) {
-        // the prefetch warp: the planners hand over the sorted miss list (named barrier 2, which they
-        // pass on every path, also a rejected one); the rows were bounds-checked against the pool
-        // allocation, so the prefetches may run before validation has finished
-        asm volatile("bar.sync 2, %0;" ::"r"(NT + 32) : "memory");
-        const int npf = (int)pf_count_sh;
-        const uint8_t* src = d.pool + (size_t)u * d.T_max * d.row_bytes;
-        for (int j = tid - NT; j < npf; j += 32)
-            prefetch_l2(src + (size_t)(sm.miss[j] >> 32) * d.row_bytes, (uint32_t)d.row_bytes);
-        finish_call(d);  // the CTA's one meeting of all its threads
-        return;
-    }
 
     if (r_ok) {
         for (int w = tid; w < SW; w += NT) {
@@ -454,13 +406,6 @@ __global__ void __launch_bounds__(kPfWarp ? kPlanThreads + 32 : kPlanThreads, MI
             }
         }
 
-        // the missing rows are known: the prefetch warp starts pulling (the
-        // first) of them over the host link while the LRU work below runs
-        if (kPfWarp) {
-            if (tid == 0) pf_count_sh = (uint32_t)(m < prefetch_rows ? m : prefetch_rows);
-            asm volatile("bar.arrive 2, %0;" ::"r"(NT + 32) : "memory");
-        }
-
         // C. victims: the first m non-hit slots in LRU order
         const int spt = (S + NT - 1) / NT;
         const int p0 = tid * spt;
@@ -500,9 +445,6 @@ __global__ void __launch_bounds__(kPfWarp ? kPlanThreads + 32 : kPlanThreads, MI
             if (s < S && (bit_test(sm.hitbits, s) || bit_test(sm.vicbits, s)) && untouched + (int)pos < S && untouched >= 0)
                 sm.lru_new[untouched + pos++] = (uint16_t)s;
         }
-    } else if (kPfWarp) {  // not a request: nothing to prefetch, but the prefetch warp waits for the count
-        if (tid == 0) pf_count_sh = 0u;
-        asm volatile("bar.arrive 2, %0;" ::"r"(NT + 32) : "memory");
     }
 
     // nothing global has been written yet; from here on the call must be known valid
@@ -665,11 +607,11 @@ cudaError_t prepare_step_kernels(int k, int S, int* gather_grid)
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(plan_kernel<true, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, plan_max);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(plan_kernel<true, 72, kFewUnitsUnroll, 1, true>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, plan_max);
+    e = cudaFuncSetAttribute(plan_kernel<true, 72, kFewUnitsUnroll, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             plan_max);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(plan_kernel<true, 0, kFewUnitsUnroll, 1, true>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, plan_max);
+    e = cudaFuncSetAttribute(plan_kernel<true, 0, kFewUnitsUnroll, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             plan_max);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(validate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)validate_smem_bytes(kMaxTopk));
@@ -708,24 +650,24 @@ cudaError_t launch_plan(const Dev& d, const int32_t* req_ids, int B, const int32
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, plan_kernel<false, 0>, d, req_ids, topk, slots, hits, misses, 0);
+    return cudaLaunchKernelEx(&cfg, plan_kernel<false, 0>, d, req_ids, topk, slots, hits, misses);
 }
 
 cudaError_t launch_plan_gather(const Dev& d, const int32_t* req_ids, int B, const int32_t* topk, int32_t* slots,
                                int32_t* hits, int32_t* misses, int device_sms, cudaStream_t st)
 {
-    // few units (at most one per SM): the variant with a prefetch warp and more
-    // loads in flight per thread.  L2 prefetch of the missing rows pays only
-    // there (planning is otherwise exposed); with more units the link is kept
-    // busy by other CTAs and the prefetched lines compete with the streaming
-    // gather: measured -1.5 % to -4 % for units in waves, and 3.22 against
-    // 3.12 ms a step for eight layer calls of 192 co-resident units.
+    // few units (at most one per SM): the variant with more loads in flight
+    // per thread, each CTA alone on its SM.  No variant prefetches the missing
+    // rows into L2 ahead of the gather: measured -1.5 % to -4 % for units in
+    // waves, 3.22 against 3.12 ms a step for eight layer calls of 192
+    // co-resident units, and for few units (a warp of its own issuing the
+    // prefetches while the CTA planned) 231.6 against 227.5 us a step at c4
+    // and 60.0 against 60.1 us at c5.
     const int grid = call_units(d, B);
     const bool few = grid <= device_sms;
-    const int prefetch_rows = few ? (int)((kPrefetchBudgetBytes / d.row_bytes) / grid) : 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(few ? kPlanThreads + 32 : kPlanThreads);
+    cfg.blockDim = dim3(kPlanThreads);
     cfg.dynamicSmemBytes = plan_smem_bytes(d.k, d.S);
     cfg.stream = st;
     // Programmatic dependent launch (planning overlaps validation) only for
@@ -740,13 +682,11 @@ cudaError_t launch_plan_gather(const Dev& d, const int32_t* req_ids, int B, cons
     cfg.attrs = attr;
     cfg.numAttrs = few ? 1 : 0;
     if (d.row_bytes == 1152)
-        return few ? cudaLaunchKernelEx(&cfg, plan_kernel<true, 72, kFewUnitsUnroll, 1, true>, d, req_ids, topk, slots,
-                                        hits, misses, prefetch_rows)
-                   : cudaLaunchKernelEx(&cfg, plan_kernel<true, 72>, d, req_ids, topk, slots, hits, misses,
-                                        prefetch_rows);
-    return few ? cudaLaunchKernelEx(&cfg, plan_kernel<true, 0, kFewUnitsUnroll, 1, true>, d, req_ids, topk, slots, hits,
-                                    misses, prefetch_rows)
-               : cudaLaunchKernelEx(&cfg, plan_kernel<true, 0>, d, req_ids, topk, slots, hits, misses, prefetch_rows);
+        return few ? cudaLaunchKernelEx(&cfg, plan_kernel<true, 72, kFewUnitsUnroll, 1>, d, req_ids, topk, slots, hits,
+                                        misses)
+                   : cudaLaunchKernelEx(&cfg, plan_kernel<true, 72>, d, req_ids, topk, slots, hits, misses);
+    return few ? cudaLaunchKernelEx(&cfg, plan_kernel<true, 0, kFewUnitsUnroll, 1>, d, req_ids, topk, slots, hits, misses)
+               : cudaLaunchKernelEx(&cfg, plan_kernel<true, 0>, d, req_ids, topk, slots, hits, misses);
 }
 
 cudaError_t launch_gather(const Dev& d, int grid, cudaStream_t st)

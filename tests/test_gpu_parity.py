@@ -58,11 +58,11 @@ def test_ragged_and_edge_workloads(w):
 
 @pytest.mark.parametrize("B,L", [(38, 4), (50, 6), (60, 9)], ids=["152_units", "300_units", "540_units"])
 def test_launch_regimes_by_unit_count(B, L):
-    """The fused kernel's three launch regimes: at most one unit per SM (a
-    prefetch warp, the kernel starting while validation runs), more units than
-    SMs but all resident at once (in-line L2 prefetch), and more than fit at
-    once (units in waves) -- each bit-exact against the oracle, with state
-    compared at the end."""
+    """The fused kernel's three launch regimes: at most one unit per SM (one
+    CTA to an SM with more loads in flight, the kernel starting while
+    validation runs), more units than SMs but all resident at once, and more
+    than fit at once (units in waves) -- each bit-exact against the oracle,
+    with state compared at the end."""
     w = wl.Workload(f"regime_{B * L}", B=B, L=L, ctx=2500, k=192, S=320, steps=4, fresh=0.3,
                     order=wl.ORDER_SHUFFLED, n_pad=5)
     p = Pair(w)
