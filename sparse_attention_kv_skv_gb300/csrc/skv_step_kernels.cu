@@ -22,12 +22,18 @@ constexpr uint32_t kEmpty = 0xFFFFFFFFu;
 constexpr int kMaxIpt = kMaxTopk / kPlanThreads;  // Top-k entries per plan thread
 
 // ---------------------------------------------------------------------------
-// The CTA's threads and how they synchronise (__syncthreads).
+// Threads that synchronise together: the whole CTA (__syncthreads), or the
+// warps [base / 32, (base + n) / 32) on named barrier 1.
 // ---------------------------------------------------------------------------
 struct CtaSync {
     int n;  // blockDim.x (a multiple of 32)
+    static constexpr int base = 0;
     __device__ __forceinline__ void sync() const { __syncthreads(); }
     __device__ __forceinline__ bool any(bool p) const { return __syncthreads_or(p) != 0; }
+};
+struct WarpGroupSync {
+    int n, base;  // multiples of 32
+    __device__ __forceinline__ void sync() const { asm volatile("bar.sync 1, %0;" ::"r"(n) : "memory"); }
 };
 
 // ---------------------------------------------------------------------------
@@ -37,7 +43,8 @@ struct CtaSync {
 template <class Sync>
 __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* total, uint32_t* sh, const Sync& sy)
 {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = sy.n >> 5;
+    const int rt = (int)threadIdx.x - sy.base;
+    const int lane = rt & 31, warp = rt >> 5, nw = sy.n >> 5;
     uint32_t x = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -67,7 +74,8 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* total,
 template <class Sync>
 __device__ __forceinline__ int32_t block_excl_max(int32_t v, int32_t* sh, const Sync& sy)
 {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = sy.n >> 5;
+    const int rt = (int)threadIdx.x - sy.base;
+    const int lane = rt & 31, warp = rt >> 5, nw = sy.n >> 5;
     int32_t x = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -280,6 +288,7 @@ __device__ __forceinline__ void finish_call(const Dev& d)
 // L2 first).
 constexpr int kFusedUnroll = 4;
 constexpr int kFewUnitsUnroll = 8;
+constexpr int kFewUnitsSplitWarps = 4;  // of the 16: the LRU order and map writes beside the gather
 
 // kFused = false: the misses become jobs of the global work list, copied by
 // gather_kernel.  kFused = true: the CTA copies its own misses (pool row ->
@@ -296,11 +305,21 @@ constexpr int kFewUnitsUnroll = 8;
 //
 // UNR: 16-byte loads in flight per thread in the gather; MINB: CTAs per SM the
 // register budget is sized for (3 when units run in waves, 1 for few units).
-template <bool kFused, int CPR_CONST, int UNR = kFusedUnroll, int MINB = 3>
+//
+// kSplitWarps > 0 (few units, where no other CTA keeps the link busy while
+// this one plans): as soon as the victims are known (phase C) and the call is
+// accepted, the first warps start the gather, and the last kSplitWarps warps
+// compute the new LRU order (D) and write the maps and outputs (E) beside it,
+// synchronising among themselves on named barrier 1.  The gather needs only
+// the sorted misses and their victim slots, and nothing outside this CTA
+// reads what D and E write before the call commits.
+template <bool kFused, int CPR_CONST, int UNR = kFusedUnroll, int MINB = 3, int kSplitWarps = 0>
 __global__ void __launch_bounds__(kPlanThreads, MINB)
     plan_kernel(Dev d, const int32_t* __restrict__ req_ids, const int32_t* __restrict__ topk,
                 int32_t* __restrict__ slots_out, int32_t* __restrict__ hits_out, int32_t* __restrict__ misses_out)
 {
+    static_assert(kSplitWarps == 0 || kFused, "the split gathers: fused kernel only");
+    static_assert(kSplitWarps >= 0 && kSplitWarps < kPlanThreads / 32, "some warps must gather");
     extern __shared__ __align__(16) uint8_t smem_raw[];
     __shared__ uint32_t scan_sh[32];
     __shared__ uint32_t job_base_sh;
@@ -325,6 +344,27 @@ __global__ void __launch_bounds__(kPlanThreads, MINB)
     const int ipt = (k + NT - 1) / NT;
     const int i0 = tid * ipt;
     int m = 0, h = 0;
+
+    // D. the slots used by this step go to the back of the LRU order, by slot
+    // index (after phase C), by the n threads of `gs`, this one being number rt
+    auto new_lru_order = [&](const auto& gs, int rt) {
+        const int spt = (S + gs.n - 1) / gs.n;
+        const int p0 = rt * spt;
+        const int untouched = S - h - m;
+        uint32_t cnt3 = 0;
+        for (int j = 0; j < spt; ++j) {
+            const int s = p0 + j;
+            if (s < S && (bit_test(sm.hitbits, s) || bit_test(sm.vicbits, s))) ++cnt3;
+        }
+        uint32_t tot3;
+        uint32_t pos = block_excl_scan(cnt3, &tot3, scan_sh, gs);
+        for (int j = 0; j < spt; ++j) {
+            const int s = p0 + j;
+            if (s < S && (bit_test(sm.hitbits, s) || bit_test(sm.vicbits, s)) && untouched + (int)pos < S &&
+                untouched >= 0)
+                sm.lru_new[untouched + pos++] = (uint16_t)s;
+        }
+    };
 
     if (r_ok) {
         for (int w = tid; w < SW; w += NT) {
@@ -431,20 +471,7 @@ __global__ void __launch_bounds__(kPlanThreads, MINB)
         }
         sy.sync();
 
-        // D. the slots used by this step go to the back, by slot index
-        const int untouched = S - h - m;
-        uint32_t cnt3 = 0;
-        for (int j = 0; j < spt; ++j) {
-            const int s = p0 + j;
-            if (s < S && (bit_test(sm.hitbits, s) || bit_test(sm.vicbits, s))) ++cnt3;
-        }
-        uint32_t tot3;
-        uint32_t pos = block_excl_scan(cnt3, &tot3, scan_sh, sy);
-        for (int j = 0; j < spt; ++j) {
-            const int s = p0 + j;
-            if (s < S && (bit_test(sm.hitbits, s) || bit_test(sm.vicbits, s)) && untouched + (int)pos < S && untouched >= 0)
-                sm.lru_new[untouched + pos++] = (uint16_t)s;
-        }
+        if (kSplitWarps == 0) new_lru_order(sy, tid);
     }
 
     // nothing global has been written yet; from here on the call must be known valid
@@ -460,54 +487,57 @@ __global__ void __launch_bounds__(kPlanThreads, MINB)
     }
     const uint32_t now1 = d.ctl[CTL_CLOCK] + 1u;
 
-    // E. stamps, map update and slot emission (plus gather jobs on the job-list path)
-    for (int i = tid; i < k; i += NT) {
-        const int32_t s = sm.out[i];
-        if (s >= 0) tsu[s] = now1;  // hit
-    }
-    if (!kFused && tid == 0) job_base_sh = m ? atomicAdd(&d.ctl[CTL_JOBS], (uint32_t)m) : 0u;
-    sy.sync();
-    for (int j = tid; j < m; j += NT) {
-        const int v = sm.victim[j];
-        const unsigned long long key = sm.miss[j];
-        const int32_t t = (int32_t)(key >> 32);
-        const int i = (int)(key & 0xFFFFFFFFu);
-        const int32_t old = s2t[v];
-        if (old >= 0) t2s[old] = -1;
-        s2t[v] = t;
-        t2s[t] = v;
-        tsu[v] = now1;
-        sm.out[i] = v;
-        if (!kFused) d.jobs[job_base_sh + j] = make_uint2((uint32_t)(u * d.T_max + t), (uint32_t)(u * S + v));
-    }
-    sy.sync();
+    // E. stamps, map update and slot emission (plus gather jobs on the job-list
+    // path), by the n threads of `gs`, this one being number rt
+    auto commit_unit = [&](const auto& gs, int rt) {
+        const int n = gs.n;
+        for (int i = rt; i < k; i += n) {
+            const int32_t s = sm.out[i];
+            if (s >= 0) tsu[s] = now1;  // hit
+        }
+        if (!kFused && rt == 0) job_base_sh = m ? atomicAdd(&d.ctl[CTL_JOBS], (uint32_t)m) : 0u;
+        gs.sync();
+        for (int j = rt; j < m; j += n) {
+            const int v = sm.victim[j];
+            const unsigned long long key = sm.miss[j];
+            const int32_t t = (int32_t)(key >> 32);
+            const int i = (int)(key & 0xFFFFFFFFu);
+            const int32_t old = s2t[v];
+            if (old >= 0) t2s[old] = -1;
+            s2t[v] = t;
+            t2s[t] = v;
+            tsu[v] = now1;
+            sm.out[i] = v;
+            if (!kFused) d.jobs[job_base_sh + j] = make_uint2((uint32_t)(u * d.T_max + t), (uint32_t)(u * S + v));
+        }
+        gs.sync();  // also orders D's writes of the new LRU order before its copy below
+        for (int i = rt; i < k; i += n) out[i] = sm.out[i];
+        if ((S & 7) == 0) {
+            const uint4* src = reinterpret_cast<const uint4*>(sm.lru_new);
+            uint4* dst = reinterpret_cast<uint4*>(lru);
+            for (int p = rt; p < S / 8; p += n) dst[p] = src[p];
+        } else {
+            for (int p = rt; p < S; p += n) lru[p] = sm.lru_new[p];
+        }
+        if (rt == 0) {
+            hits_out[blockIdx.x] = h;
+            misses_out[blockIdx.x] = m;
+            if (h) atomicAdd(&d.stats[STAT_HITS], (unsigned long long)h);
+            if (kFused && m) atomicAdd(&d.stats[STAT_MISSES], (unsigned long long)m);
+        }
+    };
 
-    for (int i = tid; i < k; i += NT) out[i] = sm.out[i];
-    if ((S & 7) == 0) {
-        const uint4* src = reinterpret_cast<const uint4*>(sm.lru_new);
-        uint4* dst = reinterpret_cast<uint4*>(lru);
-        for (int p = tid; p < S / 8; p += NT) dst[p] = src[p];
-    } else {
-        for (int p = tid; p < S; p += NT) lru[p] = sm.lru_new[p];
-    }
-    if (tid == 0) {
-        hits_out[blockIdx.x] = h;
-        misses_out[blockIdx.x] = m;
-        if (h) atomicAdd(&d.stats[STAT_HITS], (unsigned long long)h);
-        if (kFused && m) atomicAdd(&d.stats[STAT_MISSES], (unsigned long long)m);
-    }
-
-    if (kFused) {
-        // F. gather: pool row (u, token) -> hot row (u, victim slot)
+    // F. gather: pool row (u, token) -> hot row (u, victim slot), by n threads
+    auto gather = [&](int rt, int n) {
         const int4* __restrict__ src = reinterpret_cast<const int4*>(d.pool) + (size_t)u * d.T_max * cpr;
         int4* __restrict__ dst = reinterpret_cast<int4*>(d.hot) + (size_t)u * S * cpr;
         const int chunks = m * cpr;
-        for (int base = tid; base < chunks; base += NT * UNR) {
+        for (int base = rt; base < chunks; base += n * UNR) {
             int4 v[UNR];
             uint32_t o[UNR];  // victim * cpr + w < S * cpr <= 2^14 * 2^12
 #pragma unroll
             for (int j = 0; j < UNR; ++j) {
-                const int c = base + j * NT;
+                const int c = base + j * n;
                 if (c < chunks) {
                     const int jj = c / cpr;
                     const int w = c - jj * cpr;
@@ -518,10 +548,24 @@ __global__ void __launch_bounds__(kPlanThreads, MINB)
             }
 #pragma unroll
             for (int j = 0; j < UNR; ++j)
-                if (base + j * NT < chunks) st_stream(dst + o[j], v[j]);
+                if (base + j * n < chunks) st_stream(dst + o[j], v[j]);
         }
-        finish_call(d);
+    };
+
+    if (kSplitWarps > 0) {
+        constexpr int kGatherThreads = kPlanThreads - 32 * kSplitWarps;
+        if (tid < kGatherThreads) {
+            gather(tid, kGatherThreads);
+        } else {
+            const WarpGroupSync gs{NT - kGatherThreads, kGatherThreads};
+            new_lru_order(gs, tid - kGatherThreads);
+            commit_unit(gs, tid - kGatherThreads);
+        }
+    } else {
+        commit_unit(sy, tid);
+        if (kFused) gather(tid, NT);
     }
+    if (kFused) finish_call(d);
 }
 
 // ---------------------------------------------------------------------------
@@ -607,11 +651,11 @@ cudaError_t prepare_step_kernels(int k, int S, int* gather_grid)
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(plan_kernel<true, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, plan_max);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(plan_kernel<true, 72, kFewUnitsUnroll, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             plan_max);
+    e = cudaFuncSetAttribute(plan_kernel<true, 72, kFewUnitsUnroll, 1, kFewUnitsSplitWarps>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, plan_max);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(plan_kernel<true, 0, kFewUnitsUnroll, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             plan_max);
+    e = cudaFuncSetAttribute(plan_kernel<true, 0, kFewUnitsUnroll, 1, kFewUnitsSplitWarps>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, plan_max);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(validate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)validate_smem_bytes(kMaxTopk));
@@ -682,10 +726,11 @@ cudaError_t launch_plan_gather(const Dev& d, const int32_t* req_ids, int B, cons
     cfg.attrs = attr;
     cfg.numAttrs = few ? 1 : 0;
     if (d.row_bytes == 1152)
-        return few ? cudaLaunchKernelEx(&cfg, plan_kernel<true, 72, kFewUnitsUnroll, 1>, d, req_ids, topk, slots, hits,
-                                        misses)
+        return few ? cudaLaunchKernelEx(&cfg, plan_kernel<true, 72, kFewUnitsUnroll, 1, kFewUnitsSplitWarps>, d,
+                                        req_ids, topk, slots, hits, misses)
                    : cudaLaunchKernelEx(&cfg, plan_kernel<true, 72>, d, req_ids, topk, slots, hits, misses);
-    return few ? cudaLaunchKernelEx(&cfg, plan_kernel<true, 0, kFewUnitsUnroll, 1>, d, req_ids, topk, slots, hits, misses)
+    return few ? cudaLaunchKernelEx(&cfg, plan_kernel<true, 0, kFewUnitsUnroll, 1, kFewUnitsSplitWarps>, d, req_ids,
+                                    topk, slots, hits, misses)
                : cudaLaunchKernelEx(&cfg, plan_kernel<true, 0>, d, req_ids, topk, slots, hits, misses);
 }
 
