@@ -253,8 +253,8 @@ def hbm_peak_gbs():
 # dram__bytes_read.sum + dram__bytes_write.sum.  Valid only while the kernel
 # source is the one that was captured; scaled to other workloads by units.
 PROFILED_TRAFFIC = {"source": "sparse_attention_kv_skv_gb300/csrc/skv_step_kernels.cu",
-                    "sha256": "eed49c1d4efef205528b57a6de76526069b7a967d464dc9ac30ded9040a642c2",
-                    "units": 512, "dram_bytes": 42.48064e6 + 194.504192e6}
+                    "sha256": "8609ec442f09a656f3b3377eb48324f9d3c39a160a2ee9820bb5c872e1aad04a",
+                    "units": 512, "dram_bytes": 42.912768e6 + 194.209536e6}
 
 
 def profiled_traffic(w: wl.Workload):
