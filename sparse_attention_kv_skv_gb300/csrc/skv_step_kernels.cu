@@ -288,7 +288,14 @@ __device__ __forceinline__ void finish_call(const Dev& d)
 // L2 first).
 constexpr int kFusedUnroll = 4;
 constexpr int kFewUnitsUnroll = 8;
-constexpr int kFewUnitsSplitWarps = 4;  // of the 16: the LRU order and map writes beside the gather
+// of the 16 warps, those that write the LRU order and the maps beside the
+// gather (see plan_kernel): measured in one process, steps alternating between
+// variants, for few units (c4, c5) and for the 192 co-resident units of a
+// target layer call (3.075 ms a step for the eight calls without the split,
+// 3.042 with 2 or 4 warps); for units in waves it neither costs nor gains
+// (2.932 / 2.925 ms at the target, 2.826 / 2.819 at c3)
+constexpr int kFusedSplitWarps = 2;
+constexpr int kFewUnitsSplitWarps = 4;
 
 // kFused = false: the misses become jobs of the global work list, copied by
 // gather_kernel.  kFused = true: the CTA copies its own misses (pool row ->
@@ -306,13 +313,13 @@ constexpr int kFewUnitsSplitWarps = 4;  // of the 16: the LRU order and map writ
 // UNR: 16-byte loads in flight per thread in the gather; MINB: CTAs per SM the
 // register budget is sized for (3 when units run in waves, 1 for few units).
 //
-// kSplitWarps > 0 (few units, where no other CTA keeps the link busy while
-// this one plans): as soon as the victims are known (phase C) and the call is
+// kSplitWarps > 0: as soon as the victims are known (phase C) and the call is
 // accepted, the first warps start the gather, and the last kSplitWarps warps
 // compute the new LRU order (D) and write the maps and outputs (E) beside it,
 // synchronising among themselves on named barrier 1.  The gather needs only
 // the sorted misses and their victim slots, and nothing outside this CTA
-// reads what D and E write before the call commits.
+// reads what D and E write before the call commits.  It pays most where no
+// other CTA keeps the link busy while this one plans (every CTA resident).
 template <bool kFused, int CPR_CONST, int UNR = kFusedUnroll, int MINB = 3, int kSplitWarps = 0>
 __global__ void __launch_bounds__(kPlanThreads, MINB)
     plan_kernel(Dev d, const int32_t* __restrict__ req_ids, const int32_t* __restrict__ topk,
@@ -647,9 +654,11 @@ cudaError_t prepare_step_kernels(int k, int S, int* gather_grid)
     const int plan_max = (int)plan_smem_bytes(kMaxTopk, kMaxSlots);
     cudaError_t e = cudaFuncSetAttribute(plan_kernel<false, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, plan_max);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(plan_kernel<true, 72>, cudaFuncAttributeMaxDynamicSharedMemorySize, plan_max);
+    e = cudaFuncSetAttribute(plan_kernel<true, 72, kFusedUnroll, 3, kFusedSplitWarps>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, plan_max);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(plan_kernel<true, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, plan_max);
+    e = cudaFuncSetAttribute(plan_kernel<true, 0, kFusedUnroll, 3, kFusedSplitWarps>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, plan_max);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(plan_kernel<true, 72, kFewUnitsUnroll, 1, kFewUnitsSplitWarps>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, plan_max);
@@ -728,10 +737,12 @@ cudaError_t launch_plan_gather(const Dev& d, const int32_t* req_ids, int B, cons
     if (d.row_bytes == 1152)
         return few ? cudaLaunchKernelEx(&cfg, plan_kernel<true, 72, kFewUnitsUnroll, 1, kFewUnitsSplitWarps>, d,
                                         req_ids, topk, slots, hits, misses)
-                   : cudaLaunchKernelEx(&cfg, plan_kernel<true, 72>, d, req_ids, topk, slots, hits, misses);
+                   : cudaLaunchKernelEx(&cfg, plan_kernel<true, 72, kFusedUnroll, 3, kFusedSplitWarps>, d, req_ids,
+                                        topk, slots, hits, misses);
     return few ? cudaLaunchKernelEx(&cfg, plan_kernel<true, 0, kFewUnitsUnroll, 1, kFewUnitsSplitWarps>, d, req_ids,
                                     topk, slots, hits, misses)
-               : cudaLaunchKernelEx(&cfg, plan_kernel<true, 0>, d, req_ids, topk, slots, hits, misses);
+               : cudaLaunchKernelEx(&cfg, plan_kernel<true, 0, kFusedUnroll, 3, kFusedSplitWarps>, d, req_ids, topk,
+                                    slots, hits, misses);
 }
 
 cudaError_t launch_gather(const Dev& d, int grid, cudaStream_t st)
