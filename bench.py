@@ -253,8 +253,8 @@ def hbm_peak_gbs():
 # dram__bytes_read.sum + dram__bytes_write.sum.  Valid only while the kernel
 # source is the one that was captured; scaled to other workloads by units.
 PROFILED_TRAFFIC = {"source": "sparse_attention_kv_skv_gb300/csrc/skv_step_kernels.cu",
-                    "sha256": "8609ec442f09a656f3b3377eb48324f9d3c39a160a2ee9820bb5c872e1aad04a",
-                    "units": 512, "dram_bytes": 42.912768e6 + 194.209536e6}
+                    "sha256": "a1c19430ff83823c0212b4bcb0174ae49e7f3486deea95ec7cee735cd3d47927",
+                    "units": 512, "dram_bytes": 42.81984e6 + 193.69856e6}
 
 
 def profiled_traffic(w: wl.Workload):
