@@ -358,18 +358,33 @@ __global__ void __launch_bounds__(kPlanThreads, MINB)
         const int spt = (S + gs.n - 1) / gs.n;
         const int p0 = rt * spt;
         const int untouched = S - h - m;
+        // whole 32-slot words of the bitmaps when the runs tile S in words
+        const bool words = (spt & 31) == 0 && spt * gs.n == S;
         uint32_t cnt3 = 0;
-        for (int j = 0; j < spt; ++j) {
-            const int s = p0 + j;
-            if (s < S && (bit_test(sm.hitbits, s) || bit_test(sm.vicbits, s))) ++cnt3;
+        if (words) {
+            for (int w = p0 >> 5; w < (p0 + spt) >> 5; ++w) cnt3 += __popc(sm.hitbits[w] | sm.vicbits[w]);
+        } else {
+            for (int j = 0; j < spt; ++j) {
+                const int s = p0 + j;
+                if (s < S && (bit_test(sm.hitbits, s) || bit_test(sm.vicbits, s))) ++cnt3;
+            }
         }
         uint32_t tot3;
         uint32_t pos = block_excl_scan(cnt3, &tot3, scan_sh, gs);
-        for (int j = 0; j < spt; ++j) {
-            const int s = p0 + j;
-            if (s < S && (bit_test(sm.hitbits, s) || bit_test(sm.vicbits, s)) && untouched + (int)pos < S &&
-                untouched >= 0)
-                sm.lru_new[untouched + pos++] = (uint16_t)s;
+        if (words) {
+            for (int w = p0 >> 5; w < (p0 + spt) >> 5; ++w) {
+                for (uint32_t bits = sm.hitbits[w] | sm.vicbits[w]; bits != 0u; bits &= bits - 1u) {
+                    const int s = w * 32 + __ffs(bits) - 1;  // ascending within the word
+                    if (untouched + (int)pos < S && untouched >= 0) sm.lru_new[untouched + pos++] = (uint16_t)s;
+                }
+            }
+        } else {
+            for (int j = 0; j < spt; ++j) {
+                const int s = p0 + j;
+                if (s < S && (bit_test(sm.hitbits, s) || bit_test(sm.vicbits, s)) && untouched + (int)pos < S &&
+                    untouched >= 0)
+                    sm.lru_new[untouched + pos++] = (uint16_t)s;
+            }
         }
     };
 
@@ -453,21 +468,30 @@ __global__ void __launch_bounds__(kPlanThreads, MINB)
             }
         }
 
-        // C. victims: the first m non-hit slots in LRU order
+        // C. victims: the first m non-hit slots in LRU order.  Each thread
+        // takes a contiguous run of positions, read eight at a time (one
+        // 16-byte load) when the runs tile the order exactly.
         const int spt = (S + NT - 1) / NT;
         const int p0 = tid * spt;
+        const bool vec = (spt & 7) == 0 && spt * NT == S;
         uint32_t cnt = 0;
-        for (int j = 0; j < spt; ++j) {
-            const int p = p0 + j;
-            if (p < S && !bit_test(sm.hitbits, sm.lru_old[p])) ++cnt;
+        if (vec) {
+            for (int j = 0; j < spt; j += 8) {
+                const uint4 q = *reinterpret_cast<const uint4*>(sm.lru_old + p0 + j);
+                const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                for (int e = 0; e < 8; ++e) cnt += bit_test(sm.hitbits, (w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu) ? 0u : 1u;
+            }
+        } else {
+            for (int j = 0; j < spt; ++j) {
+                const int p = p0 + j;
+                if (p < S && !bit_test(sm.hitbits, sm.lru_old[p])) ++cnt;
+            }
         }
         uint32_t tot2;
         uint32_t rank = block_excl_scan(cnt, &tot2, scan_sh, sy);
-        for (int j = 0; j < spt; ++j) {
-            const int p = p0 + j;
-            if (p >= S) break;
-            const int s = sm.lru_old[p];
-            if (bit_test(sm.hitbits, s)) continue;
+        auto take = [&](int s) {  // slot s at the next position in LRU order
+            if (bit_test(sm.hitbits, s)) return;
             if ((int)rank < m) {
                 sm.victim[rank] = (uint16_t)s;
                 atomicOr(&sm.vicbits[s >> 5], 1u << (s & 31));
@@ -475,6 +499,20 @@ __global__ void __launch_bounds__(kPlanThreads, MINB)
                 sm.lru_new[rank - m] = (uint16_t)s;
             }
             ++rank;
+        };
+        if (vec) {
+            for (int j = 0; j < spt; j += 8) {
+                const uint4 q = *reinterpret_cast<const uint4*>(sm.lru_old + p0 + j);
+                const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                for (int e = 0; e < 8; ++e) take((int)((w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu));
+            }
+        } else {
+            for (int j = 0; j < spt; ++j) {
+                const int p = p0 + j;
+                if (p >= S) break;
+                take(sm.lru_old[p]);
+            }
         }
         sy.sync();
 
