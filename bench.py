@@ -253,8 +253,8 @@ def hbm_peak_gbs():
 # dram__bytes_read.sum + dram__bytes_write.sum.  Valid only while the kernel
 # source is the one that was captured; scaled to other workloads by units.
 PROFILED_TRAFFIC = {"source": "sparse_attention_kv_skv_gb300/csrc/skv_step_kernels.cu",
-                    "sha256": "a1c19430ff83823c0212b4bcb0174ae49e7f3486deea95ec7cee735cd3d47927",
-                    "units": 512, "dram_bytes": 42.81984e6 + 193.69856e6}
+                    "sha256": "6bfcf787581981146af6b7472546ccb699d69710b6133a69b08981936620f0db",
+                    "units": 512, "dram_bytes": 42.969856e6 + 193.712896e6}
 
 
 def profiled_traffic(w: wl.Workload):

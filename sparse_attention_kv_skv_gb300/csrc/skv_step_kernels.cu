@@ -289,11 +289,13 @@ __device__ __forceinline__ void finish_call(const Dev& d)
 constexpr int kFusedUnroll = 4;
 constexpr int kFewUnitsUnroll = 8;
 // of the 16 warps, those that write the LRU order and the maps beside the
-// gather (see plan_kernel): measured in one process, steps alternating between
-// variants, for few units (c4, c5) and for the 192 co-resident units of a
-// target layer call (3.075 ms a step for the eight calls without the split,
-// 3.042 with 2 or 4 warps); for units in waves it neither costs nor gains
-// (2.932 / 2.925 ms at the target, 2.826 / 2.819 at c3)
+// gather (see plan_kernel).  Measured in one process, steps alternating
+// between variants: for few units (128K context, 32 x 4 units: 226.8 us a step
+// without the split, 222.7 with 4 warps; 1M context, 4 x 4 units: 60.1 and
+// 54.5 us), for the 192 co-resident units of a layer call (16K context, batch
+// 192: 3.075 ms a step for eight calls without the split, 3.042 with 2 or 4
+// warps); for units in waves it neither costs nor gains (16K context, 192 x 8
+// units: 2.932 / 2.925 ms; the same with 40 % fresh tokens: 2.826 / 2.819)
 constexpr int kFusedSplitWarps = 2;
 constexpr int kFewUnitsSplitWarps = 4;
 
@@ -752,8 +754,8 @@ cudaError_t launch_plan_gather(const Dev& d, const int32_t* req_ids, int B, cons
     // rows into L2 ahead of the gather: measured -1.5 % to -4 % for units in
     // waves, 3.22 against 3.12 ms a step for eight layer calls of 192
     // co-resident units, and for few units (a warp of its own issuing the
-    // prefetches while the CTA planned) 231.6 against 227.5 us a step at c4
-    // and 60.0 against 60.1 us at c5.
+    // prefetches while the CTA planned) 231.6 against 227.5 us a step at 128K
+    // context (32 x 4 units) and 60.0 against 60.1 us at 1M (4 x 4 units).
     const int grid = call_units(d, B);
     const bool few = grid <= device_sms;
     cudaLaunchConfig_t cfg = {};
