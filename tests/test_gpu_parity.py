@@ -56,14 +56,20 @@ def test_ragged_and_edge_workloads(w):
     run(w)
 
 
-@pytest.mark.parametrize("B,L", [(38, 4), (50, 6), (60, 9)], ids=["152_units", "300_units", "540_units"])
-def test_launch_regimes_by_unit_count(B, L):
+@pytest.mark.parametrize("B,L,S", [(38, 4, 320), (50, 6, 320), (60, 9, 320), (38, 4, 4096), (50, 6, 4096)],
+                         ids=["152_units", "300_units", "540_units", "152_units_S4096", "300_units_S4096"])
+def test_launch_regimes_by_unit_count(B, L, S):
     """The fused kernel's three launch regimes: at most one unit per SM (one
     CTA to an SM with more loads in flight, the kernel starting while
     validation runs), more units than SMs but all resident at once, and more
     than fit at once (units in waves) -- each bit-exact against the oracle,
-    with state compared at the end."""
-    w = wl.Workload(f"regime_{B * L}", B=B, L=L, ctx=2500, k=192, S=320, steps=4, fresh=0.3,
+    with state compared at the end.  In every regime a few warps write the LRU
+    order and the maps while the others gather; with S = 4096 the victim
+    selection reads the LRU order 16 bytes at a time and the new order is built
+    from whole bitmap words (S = 320 takes the one-slot-at-a-time paths)."""
+    # with S = 4096, k = 2048 and 60 % fresh tokens a step fill the hot buffer by the third step
+    k, steps, fresh = (192, 4, 0.3) if S < 1024 else (2048, 5, 0.6)
+    w = wl.Workload(f"regime_{B * L}_{S}", B=B, L=L, ctx=max(2500, 2 * S), k=k, S=S, steps=steps, fresh=fresh,
                     order=wl.ORDER_SHUFFLED, n_pad=5)
     p = Pair(w)
     try:
@@ -71,6 +77,8 @@ def test_launch_regimes_by_unit_count(B, L):
             p.step(s)
         p.compare_state(reqs=[0, B // 2, B - 1])
         assert p.ctx.get_device_error() == 0
+        if S >= 1024:
+            assert p.total_misses > B * L * S  # more rows moved than slots: the later steps evicted
     finally:
         p.close()
 
